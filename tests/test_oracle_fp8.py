@@ -1,0 +1,125 @@
+"""Pins of the FP8 / Hadamard part of the oracle (numpy, CPU only)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8
+import synth
+
+
+def test_e4m3_encode_exhaustive_vs_library():
+    """Every finite bfloat16 value, clamped to +-448, encodes exactly as the
+    library's float32 -> float8_e4m3fn conversion does (RNE, ties to even)."""
+    bits = np.arange(65536, dtype=np.uint32)
+    f = (bits << 16).astype(np.uint32).view(np.float32)
+    x = np.clip(f[np.isfinite(f)], -448.0, 448.0).astype(np.float32)
+    mine = fp8.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, ref), np.count_nonzero(mine != ref)
+
+
+def test_e4m3_encode_saturates_and_rounds_half_even():
+    assert fp8.e4m3_encode([448.0])[0] == 0x7E
+    assert fp8.e4m3_encode([1e9])[0] == 0x7E            # finite overflow saturates
+    assert fp8.e4m3_encode([-1e9])[0] == 0xFE
+    assert fp8.e4m3_encode([np.nan])[0] == 0x7F
+    assert fp8.e4m3_encode([2.0 ** -10])[0] == 0x00     # half of the smallest subnormal: to even
+    assert fp8.e4m3_encode([3 * 2.0 ** -10])[0] == 0x02  # 1.5 quanta -> 2 (even)
+    assert fp8.e4m3_encode([1.0625])[0] == 0x38         # 1 + 1/16: tie between 1 and 1.125 -> 1
+
+
+def test_e4m3_decode_all_codes_vs_library():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = fp8.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    same = (mine == ref) | (np.isnan(mine) & np.isnan(ref))
+    assert same.all()
+    assert np.nanmax(mine) == 448.0 and mine[1] == 2.0 ** -9
+
+
+@pytest.mark.parametrize("d", [2, 4, 8, 16, 32, 64, 128, 256])
+def test_hadamard_is_orthogonal_up_to_d(d):
+    H = fp8.hadamard_matrix(d)
+    assert np.array_equal(H @ H.T, d * np.eye(d, dtype=np.int64))
+    assert np.array_equal(H, H.T)
+
+
+def test_hadamard_d2_closed_form():
+    assert np.array_equal(fp8.hadamard_matrix(2), np.array([[1, 1], [1, -1]]))
+    assert np.array_equal(fp8.hadamard_matrix(4)[3], np.array([1, -1, -1, 1]))
+
+
+def test_transform_leaves_attention_unchanged_gqa():
+    """(Q M)(K M)^T = Q K^T for orthogonal M shared by a query group and its
+    key/value head: oracle attention on transformed Q, K equals the raw one."""
+    B, N, Hq, Hkv, d = 1, 40, 4, 2, 16
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((B, N, Hq, d))
+    k = rng.standard_normal((B, N, Hkv, d))
+    v = rng.standard_normal((B, N, Hkv, d))
+    signs = synth.hadamard_signs(Hkv, d, seed=3).numpy()
+    qt = fp8.incoherent_transform(q, signs)
+    kt = fp8.incoherent_transform(k, signs)
+    o1, l1 = oracle.attention_full(q, k, v, causal=True, scale=0.25)
+    o2, l2 = oracle.attention_full(qt, kt, v, causal=True, scale=0.25)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+    # signs that differ between a query head and its key/value head break it
+    bad = signs.copy()
+    bad[:, 0] *= -1
+    qb = fp8.incoherent_transform(q, bad)
+    o3, _ = oracle.attention_full(qb, kt, v, causal=True, scale=0.25)
+    assert np.abs(o3 - o1).max() > 1e-3
+
+
+def test_block_quantisation_properties():
+    """descale = amax / 448 per (b, h, 128-token block); every code decodes to
+    within half an E4M3 spacing of x / descale; the block maximum maps to 448;
+    an all-zero block has descale 1 and zero codes; the last block is partial."""
+    B, N, H, d = 2, 300, 3, 8
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((B, N, H, d)).astype(np.float32)
+    x[1, 128:256, 2] = 0.0                      # an all-zero block
+    codes, ds = fp8.quantize_blocks(x)
+    assert ds.shape == (B, H, 3)
+    assert ds[1, 2, 1] == 1.0 and not codes[1, 128:256, 2].any()
+    for b in range(B):
+        for h in range(H):
+            for t in range(3):
+                blk = x[b, t * 128:(t + 1) * 128, h]
+                amax = np.float32(np.abs(blk).max())
+                if amax == 0:
+                    continue
+                assert ds[b, h, t] == np.float32(amax / np.float32(448.0))
+                q = blk.astype(np.float64) / np.float64(ds[b, h, t])
+                dec = fp8.e4m3_decode(codes[b, t * 128:(t + 1) * 128, h])
+                # spacing of E4M3 at |q|: 2^(floor(log2|q|) - 3), at least 2^-9
+                e = np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6)))
+                assert np.all(np.abs(dec - q) <= 0.5 * np.exp2(e - 3) * (1 + 1e-6))
+                assert np.abs(dec).max() == 448.0
+
+
+def test_fp8_error_with_hadamard_not_worse_on_outliers():
+    """The claim on the pages (incoherent processing lowers FP8 error) holds
+    for the oracle's own quantisation on the outlier workload recipe: the
+    attention output from dequantised Hadamard-processed Q, K is no further
+    from the exact output than plain per-block FP8."""
+    B, N, H, d = 1, 512, 2, 128
+    q, k, v = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=0,
+                                outlier_frac=1e-3)
+    q, k, v = (t.double().numpy() for t in (q, k, v))
+    scale = 1 / math.sqrt(d)
+    o_ref, _ = oracle.attention_full(q, k, v, causal=False, scale=scale)
+    signs = synth.hadamard_signs(H, d, seed=0).numpy()
+    errs = {}
+    for had in (False, True):
+        cq, dq, _ = fp8.prepare(q, signs, had)
+        ck, dk, _ = fp8.prepare(k, signs, had)
+        cv, dv, _ = fp8.prepare(v, signs, False)
+        o, _ = oracle.attention_full(fp8.dequantize(cq, dq), fp8.dequantize(ck, dk),
+                                     fp8.dequantize(cv, dv), causal=False, scale=scale)
+        errs[had] = math.sqrt(np.mean((o - o_ref) ** 2))
+    assert errs[True] <= errs[False], errs
