@@ -1,0 +1,162 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The library computes exact attention
+ *     O = softmax(scale * Q K^T [+ causal mask]) V,   LSE = ln sum exp(scale * Q K^T)
+ * with a tiled, streaming softmax on tcgen05 tensor cores, never writing the
+ * score matrix to HBM.  Sources of the definition:
+ *   - "FlashAttention（V3）深度解析" (dtcms.com), section 2: S = Q K^T,
+ *     P = softmax(S), O = P V; section 11 standard_attention: the scores are
+ *     scaled by 1/sqrt(d) (here: the caller's `scale`); section 11
+ *     _apply_causal_mask: key j is visible to query i iff i >= j, indices
+ *     from 0 (top-left alignment, also when Nq != Nk); section 4.2: the
+ *     streaming max/denominator merge rule used to process key blocks one
+ *     at a time.
+ *   - LSE is not defined on the pages; it is the natural-log log-sum-exp of
+ *     the scaled, masked logits of each query row.
+ *   - FP8: section 4.3 of the same page (per-block scale, dequantisation
+ *     fused into the pipeline) and the Together AI summary card
+ *     "FlashAttention-3——利用异步与低精度加速注意力机制" (Hadamard transform
+ *     with random signs applied per head before FP8 quantisation).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout   Q, O: [B, Nq, Hq, d]; K, V: [B, Nk, Hkv, d] ("BSHD": contiguous,
+ *          d innermost), as in the pages' V layout [seqlen, heads, dim]
+ *          (section 7.4, TransposeVLayout).  LSE: [B, Hq, Nq] float32.
+ * GQA      query head h reads key/value head h / (Hq / Hkv); Hq % Hkv == 0.
+ * Pointers are DEVICE pointers owned by the caller; the library never frees
+ *          or keeps them.  q, k, v, o (and the FP8 tensors) must be 128-byte
+ *          aligned (the TMA alignment pitfall on the gsyq.cn page, section 四);
+ *          lse and the descale arrays 16-byte aligned.
+ * Streams  `stream` is a cudaStream_t (NULL = legacy default stream).  Calls
+ *          enqueue work and return without synchronising; results are valid
+ *          once the stream has reached that point.
+ * Memory   The library allocates nothing per call.  A status word and the
+ *          device properties are set up once per device on first use and
+ *          kept until the process exits.
+ * Errors   0 on success.  On a negative return nothing was launched (except
+ *          ATTN_ERR_CUDA, which reports a failed launch).  Argument errors
+ *          are detected on the host before any CUDA call.
+ * Empty    B == 0 or Nq == 0 is a valid empty problem: returns 0, launches
+ *          nothing.
+ * Threads  Entry points may be called from several host threads; the first
+ *          call on a device performs the one-time set-up.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types of Q/K/V/O for attn_fwd */
+#define ATTN_F16 0  /* IEEE binary16 */
+#define ATTN_BF16 1 /* bfloat16 */
+
+/* return codes */
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG (-1) /* null pointer, negative size, Hq % Hkv != 0,
+                                     Nk == 0 with Nq > 0, scale not finite and > 0,
+                                     flag not 0/1, size over 2^31-1 rows */
+#define ATTN_ERR_UNSUPPORTED (-2) /* head dim or dtype the kernels do not cover,
+                                     or no sm_103-class device */
+#define ATTN_ERR_MISALIGNED (-3)  /* a pointer violates the alignment rule above */
+#define ATTN_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed; see attn_strerror */
+#define ATTN_ERR_TIMEOUT (-5)     /* a kernel reported a bounded wait that expired */
+#define ATTN_ERR_DEVICE (-6)      /* a kernel reported an internal consistency error */
+
+/*
+ * attn_fwd - fused attention forward, FP16 or BF16.
+ *
+ *   q     [B, Nq, Hq, d]   dtype      (read)
+ *   k, v  [B, Nk, Hkv, d]  dtype      (read)
+ *   o     [B, Nq, Hq, d]   dtype      (written: softmax(scale Q K^T [mask]) V,
+ *                                      rounded to nearest-even)
+ *   lse   [B, Hq, Nq]      float32    (written: natural-log log-sum-exp of the
+ *                                      scaled, masked logits of each row)
+ *   d     64, 128 or 256
+ *   causal 0 or 1 (top-left aligned: key j visible to query i iff j <= i)
+ *   scale  > 0 and finite (the workloads use 1/sqrt(d))
+ *   dtype  ATTN_F16 or ATTN_BF16
+ * Arithmetic: products accumulate in FP32 (tensor memory); the softmax state
+ * (row max, row sum) is FP32; the probabilities are rounded to dtype before
+ * the P V product.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int64_t Nq, int64_t Nk, int d, int causal, float scale, int dtype,
+             void* stream);
+
+/*
+ * attn_prep_fp8 - per-block FP8 E4M3 quantisation with optional incoherent
+ * processing (Hadamard transform with random signs), one tensor per call.
+ *
+ *   x        [B, N, H, d] bfloat16 (read)
+ *   x8       written E4M3FN codes:
+ *              transpose_out == 0: [B, N, H, d]          (BSHD, like x)
+ *              transpose_out == 1: [B, H, d, Npad], Npad = N rounded up to a
+ *                                  multiple of 16; positions n >= N are zero.
+ *                                  This is the key-contiguous V layout the
+ *                                  FP8 P V product reads (the pages' V
+ *                                  transpose, section 7.4).
+ *   descale  [B, H, ceil(N/128)] float32 (written): one scale per block of
+ *            128 tokens x d of one (b, head); descale = amax / 448, or 1 for
+ *            an all-zero block.  code = E4M3_RNE_satfinite(y / descale).
+ *   signs    NULL (no transform) or [sign_heads, d] int8 of +1/-1 (device).
+ *            With signs, every row is replaced, before quantisation, by
+ *            y = (x * sigma) H_d / sqrt(d) in float32, H_d the Sylvester
+ *            Hadamard matrix and sigma the row of head h / (H / sign_heads).
+ *            Apply it to Q and K with the same signs per key/value head
+ *            (Q's sign_heads = Hkv); never to V.
+ *   d        64, 128 or 256
+ */
+int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int64_t N, int d,
+                  const int8_t* signs, int sign_heads, int transpose_out, void* stream);
+
+/*
+ * attn_fwd_fp8 - fused attention forward on FP8 E4M3 inputs.
+ *
+ *   q8        [B, Nq, Hq, d]     E4M3 codes       q_descale [B, Hq, ceil(Nq/128)]
+ *   k8        [B, Nk, Hkv, d]    E4M3 codes       k_descale [B, Hkv, ceil(Nk/128)]
+ *   v8t       [B, Hkv, d, Nkpad] E4M3 codes, Nkpad = Nk rounded up to 16, padding
+ *             zero (attn_prep_fp8 with transpose_out = 1)
+ *                                                 v_descale [B, Hkv, ceil(Nk/128)]
+ *   o         [B, Nq, Hq, d] bfloat16 (written)   lse [B, Hq, Nq] float32 (written)
+ *   d         128 or 256
+ *   hadamard  0 or 1: states whether Q and K went through the transform; the
+ *             arithmetic does not change (Q M (K M)^T = Q K^T), the flag is
+ *             validated and kept for the caller's bookkeeping.
+ * Dequantisation is fused: logits use q_descale * k_descale per 128 x 128
+ * tile; the probabilities are quantised to E4M3 for the P V product with the
+ * value block's scale folded in; sums and the output stay FP32 until the
+ * final bfloat16 rounding.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q_descale,
+                 const float* k_descale, const float* v_descale, void* o, float* lse, int B,
+                 int Hq, int Hkv, int64_t Nq, int64_t Nk, int d, int causal, float scale,
+                 int hadamard, void* stream);
+
+/*
+ * attn_get_status - synchronise `stream`, then read and clear the device
+ * status word that kernels set when a bounded wait expires (ATTN_ERR_TIMEOUT)
+ * or an internal check fails (ATTN_ERR_DEVICE).  Returns 0 if no kernel
+ * reported a problem since the last call, ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int attn_get_status(void* stream);
+
+/* attn_strerror - static text for a return code; for ATTN_ERR_CUDA the text
+ * of the last CUDA failure seen by this thread. */
+const char* attn_strerror(int code);
+
+/* attn_launch_count - number of kernels this library has launched in the
+ * process so far (monotonic; used to count launches in a timed region). */
+int64_t attn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

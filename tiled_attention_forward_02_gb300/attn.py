@@ -1,0 +1,182 @@
+"""Python binding of the C-ABI attention library (``include/attn.h``).
+
+Argument marshalling only: shape/dtype/device checks, output allocation with
+torch (device memory is plumbing), and one ctypes call per entry point on the
+current torch stream.  Every step of the computation runs in the library's
+CUDA kernels; there is no fallback of any kind.  If the shared library is
+missing, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libattn.so")
+
+ATTN_F16, ATTN_BF16 = 0, 1
+OK = 0
+ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED = -1, -2, -3
+ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = -4, -5, -6
+
+EXPORTS = ("attn_fwd", "attn_prep_fp8", "attn_fwd_fp8", "attn_get_status", "attn_strerror",
+           "attn_launch_count")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: error {code}: {strerror(code)}")
+
+
+def load():
+    """Load ``lib/libattn.so`` (built by ``build.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.attn_fwd.restype = i32
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, f32, i32, vp]
+    lib.attn_prep_fp8.restype = i32
+    lib.attn_prep_fp8.argtypes = [vp, vp, vp, i32, i32, i64, i32, vp, i32, i32, vp]
+    lib.attn_fwd_fp8.restype = i32
+    lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32,
+                                 f32, i32, vp]
+    lib.attn_get_status.restype = i32
+    lib.attn_get_status.argtypes = [vp]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_strerror.argtypes = [i32]
+    lib.attn_launch_count.restype = i64
+    lib.attn_launch_count.argtypes = []
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load().attn_strerror(int(code)).decode()
+
+
+def launch_count() -> int:
+    return int(load().attn_launch_count())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise AttnError(rc, where)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous (BSHD)")
+
+
+def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nk, d, causal, scale, dtype,
+            stream) -> int:
+    """Direct C call with raw integers (used by the boundary tests)."""
+    return load().attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nk, d, causal,
+                           scale, dtype, stream)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             stream=None):
+    """O, LSE = attention(q, k, v).  q: [B, Nq, Hq, d]; k, v: [B, Nk, Hkv, d]
+    (fp16 or bf16, contiguous, CUDA).  Returns (O [B, Nq, Hq, d], LSE [B, Hq, Nq] fp32)."""
+    _need_cuda(q, k, v)
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be float16 or all bfloat16")
+    B, Nq, Hq, d = q.shape
+    Bk, Nk, Hkv, dk = k.shape
+    if v.shape != k.shape or Bk != B or dk != d:
+        raise ValueError("shape mismatch between q, k, v")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F16
+    rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                         int(bool(causal)), float(scale), dt, _stream(stream))
+    _check(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_prep_fp8(x, signs=None, sign_heads: int | None = None, transpose_out: bool = False,
+                  out=None, descale=None, stream=None):
+    """Per-128-token-block E4M3 quantisation of x [B, N, H, d] (bf16), with the
+    optional Hadamard transform (signs [G, d] int8 +-1 on the device).
+    Returns (codes uint8, descale fp32 [B, H, ceil(N/128)]); codes are
+    [B, N, H, d], or [B, H, d, Npad] (Npad = N rounded up to 16) when
+    ``transpose_out``."""
+    _need_cuda(x)
+    if x.dtype != torch.bfloat16:
+        raise ValueError("x must be bfloat16")
+    B, N, H, d = x.shape
+    nb = (N + 127) // 128
+    if transpose_out:
+        npad = (N + 15) // 16 * 16
+        shape = (B, H, d, npad)
+    else:
+        shape = (B, N, H, d)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.uint8, device=x.device)
+    if descale is None:
+        descale = torch.empty((B, H, nb), dtype=torch.float32, device=x.device)
+    if signs is not None:
+        _need_cuda(signs)
+        if signs.dtype != torch.int8 or signs.shape[1] != d:
+            raise ValueError("signs must be int8 [G, d]")
+        sign_heads = signs.shape[0] if sign_heads is None else sign_heads
+    rc = load().attn_prep_fp8(_ptr(x), _ptr(out), _ptr(descale), B, H, N, d, _ptr(signs),
+                              int(sign_heads or 0), int(bool(transpose_out)), _stream(stream))
+    _check(rc, "attn_prep_fp8")
+    return out, descale
+
+
+def attn_fwd_fp8(q8, k8, v8t, q_descale, k_descale, v_descale, *, Hq: int | None = None,
+                 causal: bool = False, scale: float | None = None, hadamard: bool = False,
+                 out=None, lse=None, stream=None):
+    """FP8 forward.  q8 [B, Nq, Hq, d], k8 [B, Nk, Hkv, d] uint8 E4M3 codes,
+    v8t [B, Hkv, d, Nkpad]; descales fp32 per 128-token block.
+    Returns (O bf16 [B, Nq, Hq, d], LSE fp32 [B, Hq, Nq])."""
+    _need_cuda(q8, k8, v8t, q_descale, k_descale, v_descale)
+    B, Nq, Hq_, d = q8.shape
+    _, Nk, Hkv, _ = k8.shape
+    if out is None:
+        out = torch.empty((B, Nq, Hq_, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, Hq_, Nq), dtype=torch.float32, device=q8.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(q_descale), _ptr(k_descale),
+                             _ptr(v_descale), _ptr(out), _ptr(lse), B, Hq_, Hkv, Nq, Nk, d,
+                             int(bool(causal)), float(scale), int(bool(hadamard)), _stream(stream))
+    _check(rc, "attn_fwd_fp8")
+    return out, lse
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word as a code."""
+    return int(load().attn_get_status(_stream(stream)))

@@ -1,0 +1,279 @@
+// api.cu - the C ABI (include/attn.h): argument validation, one-time device
+// set-up, TMA tensor-map encoding, kernel dispatch and error reporting.
+// No torch types cross this boundary; every pointer is a plain device
+// pointer owned by the caller.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "attn_fwd_kernel.cuh"
+#include "internal.h"
+
+namespace attn {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxRows = (int64_t)1 << 30;  // TMA coordinates are int32; keep head-room
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  int smem_optin = 0;
+  unsigned int* status = nullptr;  // device status word (timeouts, internal checks)
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int64_t> g_launches{0};
+thread_local char g_cuda_msg[256] = "no CUDA error recorded";
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// one-time per-device set-up; returns 0 or an error code
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) ||
+        (e = cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        (e = cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+        (e = cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported,
+                         "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if ((e = cudaMalloc(&st.status, sizeof(unsigned int))) != cudaSuccess)
+      return cuda_fail(e, "cudaMalloc(status word)");
+    if ((e = cudaMemset(st.status, 0, sizeof(unsigned int))) != cudaSuccess)
+      return cuda_fail(e, "cudaMemset(status word)");
+    st.ready = true;
+  }
+  // the kernels are built for sm_103a only
+  if (st.cc_major != 10 || st.cc_minor != 3) return ATTN_ERR_UNSUPPORTED;
+  *out = &st;
+  return ATTN_OK;
+}
+
+int encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const cuuint64_t dims[4],
+           const cuuint64_t strides[3], const cuuint32_t box[4]) {
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_cuda_msg, sizeof(g_cuda_msg), "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+// BSHD tensor [B, N, H, d] as TMA dims (d, H, N, B); box = one head, 128 rows,
+// `inner` elements of d (128 bytes for the 128-byte swizzle)
+int map_bshd(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* base, int B, int64_t N,
+             int H, int d, int inner) {
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * esz, (cuuint64_t)H * d * esz,
+                                 (cuuint64_t)N * H * d * esz};
+  const cuuint32_t box[4] = {(cuuint32_t)inner, 1, 128, 1};
+  return encode(map, dt, base, dims, strides, box);
+}
+
+// transposed value tensor [B, H, d, Npad] (bytes) as dims (Npad, d, H, B);
+// box = 128 keys x d channels
+int map_vt(CUtensorMap* map, const void* base, int B, int H, int d, int64_t Npad) {
+  const cuuint64_t dims[4] = {(cuuint64_t)Npad, (cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)Npad, (cuuint64_t)d * Npad,
+                                 (cuuint64_t)H * d * Npad};
+  const cuuint32_t box[4] = {128, (cuuint32_t)d, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box);
+}
+
+// checks shared by both forward entry points; returns 1 for an empty problem
+int check_common(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int causal, float scale) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (Nq > kMaxRows || Nk > kMaxRows) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || Nq == 0) return 1;
+  if (Nk == 0) return ATTN_ERR_INVALID_ARG;
+  return 0;
+}
+
+int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, float scale,
+                const DeviceState& st, int* grid) {
+  const int qst = fwd_q_tiles(d);
+  const int64_t n_mb = (Nq + qst * 128 - 1) / (qst * 128);
+  const int64_t units = (int64_t)B * Hq * n_mb;
+  if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.group = Hq / Hkv;
+  p.Nq = (int)Nq;
+  p.Nk = (int)Nk;
+  p.n_kv_tiles = (int)((Nk + 127) / 128);
+  p.n_mblocks = (int)n_mb;
+  p.n_units = (int)units;
+  p.nqb = (int)((Nq + 127) / 128);
+  p.nkb = (int)((Nk + 127) / 128);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = st.status;
+  *grid = (int)(units < st.sm_count ? units : st.sm_count);
+  return ATTN_OK;
+}
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_cuda_msg, sizeof(g_cuda_msg), "%s: %s (%s)", where, cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return ATTN_ERR_CUDA;
+}
+
+int check_launch() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "kernel launch");
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Hq, int Hkv, int64_t Nq, int64_t Nk, int d, int causal, float scale,
+                        int dtype, void* stream) {
+  int rc = check_common(B, Hq, Hkv, Nq, Nk, causal, scale);
+  if (rc < 0) return rc;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (rc == 1) return ATTN_OK;  // empty problem
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 128) || !aligned(k, 128) || !aligned(v, 128) || !aligned(o, 128) ||
+      !aligned(lse, 16))
+    return ATTN_ERR_MISALIGNED;
+
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  const CUtensorMapDataType tdt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv;
+  if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64)) ||
+      (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64)) ||
+      (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64)))
+    return rc;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  int grid = 0;
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid)) != ATTN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return dtype == ATTN_BF16 ? launch_fwd_bf16(d, causal, mq, mk, mv, p, grid, s)
+                            : launch_fwd_f16(d, causal, mq, mk, mv, p, grid, s);
+}
+
+extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
+                            const float* q_descale, const float* k_descale,
+                            const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
+                            int64_t Nq, int64_t Nk, int d, int causal, float scale, int hadamard,
+                            void* stream) {
+  int rc = check_common(B, Hq, Hkv, Nq, Nk, causal, scale);
+  if (rc < 0) return rc;
+  if (hadamard != 0 && hadamard != 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (rc == 1) return ATTN_OK;
+  if (!q8 || !k8 || !v8t || !q_descale || !k_descale || !v_descale || !o || !lse)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q8, 128) || !aligned(k8, 128) || !aligned(v8t, 128) || !aligned(o, 128) ||
+      !aligned(lse, 16) || !aligned(q_descale, 16) || !aligned(k_descale, 16) ||
+      !aligned(v_descale, 16))
+    return ATTN_ERR_MISALIGNED;
+
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  const int64_t Npad = (Nk + 15) / 16 * 16;
+  CUtensorMap mq, mk, mv;
+  if ((rc = map_bshd(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q8, B, Nq, Hq, d, 128)) ||
+      (rc = map_bshd(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k8, B, Nk, Hkv, d, 128)) ||
+      (rc = map_vt(&mv, v8t, B, Hkv, d, Npad)))
+    return rc;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.q_descale = q_descale;
+  p.k_descale = k_descale;
+  p.v_descale = v_descale;
+  int grid = 0;
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid)) != ATTN_OK) return rc;
+  return launch_fwd_e4m3(d, causal, mq, mk, mv, p, grid, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int64_t N,
+                             int d, const int8_t* signs, int sign_heads, int transpose_out,
+                             void* stream) {
+  if (B < 0 || H < 1 || N < 0) return ATTN_ERR_INVALID_ARG;
+  if (transpose_out != 0 && transpose_out != 1) return ATTN_ERR_INVALID_ARG;
+  if (signs && (sign_heads < 1 || H % sign_heads != 0)) return ATTN_ERR_INVALID_ARG;
+  if (N > kMaxRows) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y/z limits
+  if (B == 0 || N == 0) return ATTN_OK;
+  if (!x || !x8 || !descale) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(x, 128) || !aligned(x8, 128) || !aligned(descale, 16)) return ATTN_ERR_MISALIGNED;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  const int group = signs ? H / sign_heads : 1;
+  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, transpose_out,
+                         static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_get_status(void* stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  if ((e = cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy(status word)");
+  if (word == 0) return ATTN_OK;
+  if ((e = cudaMemset(st->status, 0, sizeof(word))) != cudaSuccess)
+    return cuda_fail(e, "cudaMemset(status word)");
+  return (word & kStatusTimeout) ? ATTN_ERR_TIMEOUT : ATTN_ERR_DEVICE;
+}
+
+extern "C" const char* attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head dimension, element type or device";
+    case ATTN_ERR_MISALIGNED: return "pointer not aligned (128 bytes for tensors, 16 for vectors)";
+    case ATTN_ERR_CUDA: return g_cuda_msg;
+    case ATTN_ERR_TIMEOUT: return "a kernel wait expired (bounded wait timeout)";
+    case ATTN_ERR_DEVICE: return "a kernel reported an internal consistency error";
+    default: return "unknown error code";
+  }
+}
+
+extern "C" int64_t attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

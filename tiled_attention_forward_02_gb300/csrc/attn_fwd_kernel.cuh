@@ -1,0 +1,599 @@
+// attn_fwd_kernel.cuh - fused, tiled attention forward for sm_103a (tcgen05 + TMA).
+//
+// What is computed (FlashAttention（V3）深度解析, dtcms.com, sections 2, 4.2, 11):
+//   S = scale * Q K^T (+ causal mask: key j visible to query i iff j <= i),
+//   P = softmax(S) row-wise, O = P V, LSE = ln sum_j exp(S_ij),
+// with S and P never leaving the SM: each 128-key block of K/V is streamed
+// through shared memory and folded into a running FP32 (max, sum, O) per query
+// row with the merge rule m = max(m_a, m_b), z = z_a e^(m_a-m) + z_b e^(m_b-m)
+// (section 4.2).
+//
+// Blackwell mapping (the pages' Hopper design - TMA producer warps, WGMMA
+// consumers, inter-warpgroup ping-pong, section 7.3 - redone for tcgen05):
+//   * one persistent CTA per SM walks work units (b, query head, block of
+//     QST x 128 query rows); QST = 2 query tiles share every K/V tile;
+//   * load warp: one thread issues TMA copies of Q (once per unit) and of the
+//     K/V tiles into a ring of NSLOT shared-memory slots (full/empty
+//     mbarriers, 128-byte swizzle);
+//   * MMA warp: one thread issues tcgen05.mma S_s = Q_s K_j^T into tensor
+//     memory and O_s += P_s V_j with P_s read from tensor memory; stage order
+//     PV_0(j-1), S_0(j), PV_1(j-1), S_1(j) makes one tile's softmax overlap
+//     the other tile's two GEMMs (the pages' ping-pong);
+//   * softmax warpgroups (one per query tile, one thread per query row =
+//     one TMEM lane): tcgen05.ld of the S row, mask, row max, conditional
+//     rescale of O in tensor memory, exp2, row sum, P rounded to the input
+//     type and written back over S with tcgen05.st; the same warps run the
+//     epilogue (O / l, LSE) of their tile.
+// The pages' intra-warpgroup overlap and named barriers have no direct
+// counterpart: the MMA warp is asynchronous to the softmax warps by
+// construction, and mbarriers + tcgen05.commit replace the named barriers.
+//
+// Tensor memory (512 columns x 128 lanes, FP32): S_s at column 128 s,
+// O_s at 128 QST + D s.  P_s (16-bit: 64 columns, 8-bit: 32 columns) is
+// written over the first columns of S_s after S_s has been read.
+//
+// FP8 (E4M3) instance: per-128-token-block descales are applied to the
+// logits per 128 x 128 tile; P is quantised to E4M3 with the V block's scale
+// folded into the exponent (see softmax_tile); V arrives transposed
+// ([B, Hkv, d, Nkpad], keys contiguous) so both GEMMs read K-major operands.
+#pragma once
+
+#include <cuda.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+enum : int { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+
+// bit set in the device status word when a bounded wait expires
+constexpr unsigned kStatusTimeout = 1u;
+// cycles a wait may spin before the kernel gives up (about 2 s at 2 GHz)
+constexpr long long kWaitBudgetCycles = 4000000000LL;
+
+struct FwdParams {
+  void* o;                 // [B, Nq, Hq, D], f16/bf16 (bf16 for the FP8 instance)
+  float* lse;              // [B, Hq, Nq]
+  const float* q_descale;  // FP8 only: [B, Hq, nqb]
+  const float* k_descale;  //            [B, Hkv, nkb]
+  const float* v_descale;  //            [B, Hkv, nkb]
+  unsigned int* status;    // device status word
+  int B, Hq, Hkv, group;   // group = Hq / Hkv
+  int Nq, Nk;
+  int n_kv_tiles;          // ceil(Nk / 128)
+  int n_mblocks;           // ceil(Nq / (QST * 128))
+  int n_units;             // B * Hq * n_mblocks
+  int nqb, nkb;            // descale blocks per head
+  float scale_log2;        // scale * log2(e)
+};
+
+template <int D, int DT>
+struct FwdCfg {
+  static constexpr int ELT = (DT == DT_E4M3) ? 1 : 2;
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int QST = (D == 256) ? 1 : 2;   // query tiles per unit (TMEM budget)
+  static constexpr int ROWB = D * ELT;              // bytes of one Q/K row
+  static constexpr int NCH = ROWB / 128;            // 128-byte swizzle chunks per row
+  static constexpr int CH_ELEMS = 128 / ELT;        // elements per chunk
+  static constexpr int CHUNK_BYTES = 128 * 128;     // one chunk of 128 rows
+  static constexpr int QBYTES = BM * ROWB;
+  static constexpr int KVBYTES = BN * ROWB;         // K tile; V (or V^T) tile is the same size
+  static constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
+  static constexpr int SMEM_TAIL = 512;             // barriers + TMEM address + flags
+  static constexpr int SLOT_FIT = (SMEM_LIMIT - 1024 - SMEM_TAIL - QST * QBYTES) / KVBYTES;
+  static constexpr int NSLOT = SLOT_FIT > 8 ? 8 : SLOT_FIT;
+  static constexpr int SMEM_BYTES = 1024 + QST * QBYTES + NSLOT * KVBYTES + SMEM_TAIL;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int S_COL0 = 0;                  // S_s at S_COL0 + 128 s
+  static constexpr int O_COL0 = 128 * QST;          // O_s at O_COL0 + D s
+  static constexpr int NUM_WARPS = QST * 4 + 2;
+  static constexpr int NTHREADS = NUM_WARPS * 32;
+  static constexpr int W_MMA = QST * 4;
+  static constexpr int W_LOAD = QST * 4 + 1;
+  // softmax: lazy rescale threshold (log2 units) and exponent shift of P
+  static constexpr float TAU = (DT == DT_E4M3) ? 2.0f : 8.0f;
+  static constexpr float PSHIFT = (DT == DT_E4M3) ? 6.0f : 0.0f;
+
+  static_assert(NSLOT >= 2, "shared memory too small for a double-buffered K/V ring");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory over budget");
+  static_assert(O_COL0 + QST * D <= TMEM_COLS, "tensor memory over budget");
+};
+
+// ---------------------------------------------------------------- descriptors
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle (layout type 2),
+// descriptor version 1 (bits 46-47).  lbo/sbo in bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// tcgen05 instruction descriptor: FP32 accumulate, dense, A K-major.
+// fmt: 0 = f16 / e4m3, 1 = bf16 / e5m2 (per kind); b_mn_major selects a
+// transposed (N-contiguous) B operand.
+__host__ __device__ constexpr uint32_t idesc_make(uint32_t fmt, int M, int N, bool b_mn_major) {
+  return (1u << 4)                          // D format: FP32
+         | (fmt << 7)                       // A format
+         | (fmt << 10)                      // B format
+         | ((b_mn_major ? 1u : 0u) << 16)   // B major-ness
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// ----------------------------------------------------------------- scheduling
+struct Unit {
+  int b, hq, hk, m0;
+  int n_s[2];   // key tiles each query tile visits
+  int n;        // max over the tiles
+};
+
+template <int QST, bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
+  Unit U;
+  const int BH = p.B * p.Hq;
+  int mb, bh;
+  if (CAUSAL) {  // heaviest row blocks first, heads interleaved
+    mb = p.n_mblocks - 1 - u / BH;
+    bh = u % BH;
+  } else {       // head-major: concurrent CTAs share one head's K/V in L2
+    bh = u / p.n_mblocks;
+    mb = u % p.n_mblocks;
+  }
+  U.b = bh / p.Hq;
+  U.hq = bh % p.Hq;
+  U.hk = U.hq / p.group;
+  U.m0 = mb * QST * 128;
+  U.n = 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    int n = p.n_kv_tiles;
+    if (CAUSAL) {
+      const int last_row = U.m0 + s * 128 + 127;  // top-left aligned mask
+      const int need = last_row / 128 + 1;
+      n = need < n ? need : n;
+    }
+    U.n_s[s] = (s < QST) ? n : 0;
+    if (s < QST && n > U.n) U.n = n;
+  }
+  return U;
+}
+
+// unit visited by this CTA in round `it` (snake order for the causal case so
+// that the CTA that took the heaviest unit of one round takes the lightest of
+// the next); -1 when the round has no unit for this CTA, -2 when done
+template <bool CAUSAL>
+__device__ __forceinline__ int unit_of_round(int it, const FwdParams& p) {
+  const int G = gridDim.x;
+  const long long base = (long long)it * G;
+  if (base >= p.n_units) return -2;
+  const int c = (CAUSAL && (it & 1)) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+  const long long u = base + c;
+  return u < p.n_units ? (int)u : -1;
+}
+
+// ------------------------------------------------------------ bounded waits
+struct Ctl {
+  volatile int* abort_flag;
+  unsigned int* status;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*ctl.abort_flag) return false;
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      *ctl.abort_flag = 1;
+      atomicOr(ctl.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// a whole warp waits; the outcome is made warp-uniform so that the
+// warp-collective tcgen05 loads/stores that follow stay convergent
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+  const bool ok = wait_bar(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// --------------------------------------------------------------------- kernel
+template <int D, int DT, bool CAUSAL>
+__global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D, DT>;
+  constexpr int QST = C::QST;
+  constexpr int NSLOT = C::NSLOT;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sraw = ptx::smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (sraw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sQ = sraw + pad;                       // QST query tiles
+  const uint32_t sKV = sQ + QST * C::QBYTES;            // NSLOT K/V slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QST * C::QBYTES + NSLOT * C::KVBYTES);
+
+  // barrier table
+  constexpr int B_QFULL = 0;                 // [2]   TMA Q landed            (tx)
+  constexpr int B_QEMPTY = 2;                // [1]   last S GEMM of unit done (commit)
+  constexpr int B_KVFULL = 3;                // [NSLOT] TMA K/V landed        (tx)
+  constexpr int B_KVEMPTY = 3 + NSLOT;       // [NSLOT] GEMMs reading slot done (commit)
+  constexpr int B_SFULL = 3 + 2 * NSLOT;     // [2]   S_s ready               (commit)
+  constexpr int B_PFULL = B_SFULL + 2;       // [2]   P_s written, O_s rescaled (128 arrivals)
+  constexpr int B_OFULL = B_PFULL + 2;       // [2]   last PV of unit done    (commit)
+  constexpr int B_OEMPTY = B_OFULL + 2;      // [2]   epilogue read O_s       (128 arrivals)
+  constexpr int B_DRAIN = B_OEMPTY + 2;      // [1]   all MMAs of this CTA done (commit)
+  constexpr int NBARS = B_DRAIN + 1;
+  static_assert(NBARS * 8 + 16 <= C::SMEM_TAIL, "barrier table too large");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) -> uint32_t { return ptx::smem_addr(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Ctl ctl{abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar(B_QFULL + s), 1);
+      ptx::mbar_init(bar(B_SFULL + s), 1);
+      ptx::mbar_init(bar(B_PFULL + s), 128);
+      ptx::mbar_init(bar(B_OFULL + s), 1);
+      ptx::mbar_init(bar(B_OEMPTY + s), 128);
+    }
+    ptx::mbar_init(bar(B_QEMPTY), 1);
+    for (int i = 0; i < NSLOT; ++i) {
+      ptx::mbar_init(bar(B_KVFULL + i), 1);
+      ptx::mbar_init(bar(B_KVEMPTY + i), 1);
+    }
+    ptx::mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == C::W_MMA) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  if (warp == C::W_LOAD && lane == 0) {
+    ptx::tma_prefetch_desc(&tmQ);
+    ptx::tma_prefetch_desc(&tmK);
+    ptx::tma_prefetch_desc(&tmV);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::W_LOAD) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      int kv_it = 0, u_it = 0;
+      bool ok = true;
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      for (int it = 0; ok; ++it) {
+        const int u = unit_of_round<CAUSAL>(it, p);
+        if (u == -2) break;
+        if (u < 0) continue;
+        const Unit U = decode_unit<QST, CAUSAL>(u, p);
+        ok = wait_bar(bar(B_QEMPTY), (u_it & 1) ^ 1, ctl);
+        if (!ok) break;
+        for (int s = 0; s < QST; ++s) {
+          ptx::mbar_arrive_expect_tx(bar(B_QFULL + s), C::QBYTES);
+          for (int ch = 0; ch < C::NCH; ++ch)
+            ptx::tma_load_4d(sQ + s * C::QBYTES + ch * C::CHUNK_BYTES, &tmQ, bar(B_QFULL + s),
+                             ch * C::CH_ELEMS, U.hq, U.m0 + s * 128, U.b);
+        }
+        for (int j = 0; j < U.n && ok; ++j) {
+          // K_j
+          {
+            const int slot = kv_it % NSLOT;
+            ok = wait_bar(bar(B_KVEMPTY + slot), ((kv_it / NSLOT) & 1) ^ 1, ctl);
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx(bar(B_KVFULL + slot), C::KVBYTES);
+            for (int ch = 0; ch < C::NCH; ++ch)
+              ptx::tma_load_4d_hint(sKV + slot * C::KVBYTES + ch * C::CHUNK_BYTES, &tmK,
+                                    bar(B_KVFULL + slot), ch * C::CH_ELEMS, U.hk, j * 128, U.b,
+                                    pol_kv);
+            ++kv_it;
+          }
+          // V_j (FP8: one box of the transposed tensor, D rows x 128 keys)
+          {
+            const int slot = kv_it % NSLOT;
+            ok = wait_bar(bar(B_KVEMPTY + slot), ((kv_it / NSLOT) & 1) ^ 1, ctl);
+            if (!ok) break;
+            ptx::mbar_arrive_expect_tx(bar(B_KVFULL + slot), C::KVBYTES);
+            if constexpr (DT == DT_E4M3) {
+              ptx::tma_load_4d_hint(sKV + slot * C::KVBYTES, &tmV, bar(B_KVFULL + slot), j * 128,
+                                    0, U.hk, U.b, pol_kv);
+            } else {
+              for (int ch = 0; ch < C::NCH; ++ch)
+                ptx::tma_load_4d_hint(sKV + slot * C::KVBYTES + ch * C::CHUNK_BYTES, &tmV,
+                                      bar(B_KVFULL + slot), ch * C::CH_ELEMS, U.hk, j * 128, U.b,
+                                      pol_kv);
+            }
+            ++kv_it;
+          }
+        }
+        ++u_it;
+      }
+      // wait (bounded) for copies still in flight before the CTA can exit
+      const int pending = kv_it < NSLOT ? kv_it : NSLOT;
+      for (int t = kv_it - pending; t < kv_it; ++t)
+        wait_bar(bar(B_KVFULL + t % NSLOT), (t / NSLOT) & 1, Ctl{abort_flag, p.status});
+      if (u_it > 0)
+        for (int s = 0; s < QST; ++s) wait_bar(bar(B_QFULL + s), (u_it - 1) & 1, ctl);
+    }
+    __syncwarp();
+  } else if (warp == C::W_MMA) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t fmt = (DT == DT_BF16) ? 1u : 0u;
+      constexpr uint32_t idS = idesc_make(fmt, 128, 128, false);
+      constexpr uint32_t idO = idesc_make(fmt, 128, D, DT != DT_E4M3);
+      int kv_it = 0, u_it = 0;
+      int pv_cnt[2] = {0, 0};
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int u = unit_of_round<CAUSAL>(it, p);
+        if (u == -2) break;
+        if (u < 0) continue;
+        const Unit U = decode_unit<QST, CAUSAL>(u, p);
+        for (int s = 0; s < QST && ok; ++s) ok = wait_bar(bar(B_QFULL + s), u_it & 1, ctl);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        for (int j = 0; j <= U.n && ok; ++j) {
+          const int k_idx = kv_it + 2 * j;
+          const int v_idx = kv_it + 2 * j - 1;
+          const int kslot = k_idx % NSLOT;
+          const int vslot = (v_idx + NSLOT) % NSLOT;
+          if (j < U.n) ok = wait_bar(bar(B_KVFULL + kslot), (k_idx / NSLOT) & 1, ctl);
+          if (ok && j >= 1) ok = wait_bar(bar(B_KVFULL + vslot), (v_idx / NSLOT) & 1, ctl);
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int s = 0; s < QST; ++s) {
+            const uint32_t tS = tmem + C::S_COL0 + 128 * s;
+            const uint32_t tO = tmem + C::O_COL0 + D * s;
+            if (j >= 1 && j - 1 < U.n_s[s]) {
+              // O_s += P_s V_{j-1}
+              ok = wait_bar(bar(B_PFULL + s), pv_cnt[s] & 1, ctl);
+              ++pv_cnt[s];
+              if (ok && j == 1) ok = wait_bar(bar(B_OEMPTY + s), (u_it & 1) ^ 1, ctl);
+              if (!ok) break;
+              ptx::tc_fence_after();
+              const uint32_t vbase = sKV + vslot * C::KVBYTES;
+              if constexpr (DT == DT_E4M3) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)   // 32 keys per MMA, 8 TMEM columns of P
+                  ptx::mma_f8_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 32, 16, 1024), idO,
+                                 (j > 1 || kk > 0) ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)   // 16 keys per MMA, 8 TMEM columns of P
+                  ptx::mma_f16_ts(tO, tS + kk * 8,
+                                  sdesc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), idO,
+                                  (j > 1 || kk > 0) ? 1u : 0u);
+              }
+              if (j - 1 == U.n_s[s] - 1) ptx::tc_commit(bar(B_OFULL + s));
+            }
+            if (j < U.n_s[s]) {
+              // S_s = Q_s K_j^T
+              const uint32_t qbase = sQ + s * C::QBYTES;
+              const uint32_t kbase = sKV + kslot * C::KVBYTES;
+              constexpr int KSTEPS = C::ROWB / 32;   // 32 bytes of K per MMA
+#pragma unroll
+              for (int kk = 0; kk < KSTEPS; ++kk) {
+                const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                const uint64_t a = sdesc_sw128(qbase + off, 16, 1024);
+                const uint64_t b = sdesc_sw128(kbase + off, 16, 1024);
+                if constexpr (DT == DT_E4M3)
+                  ptx::mma_f8_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
+                else
+                  ptx::mma_f16_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
+              }
+              ptx::tc_commit(bar(B_SFULL + s));
+            }
+          }
+          if (!ok) break;
+          if (j < U.n) ptx::tc_commit(bar(B_KVEMPTY + kslot));
+          if (j >= 1) ptx::tc_commit(bar(B_KVEMPTY + vslot));
+          if (j == U.n - 1) ptx::tc_commit(bar(B_QEMPTY));
+        }
+        kv_it += 2 * U.n;
+        ++u_it;
+      }
+      // every MMA issued by this thread must finish before TMEM is released
+      ptx::tc_commit(bar(B_DRAIN));
+      wait_bar(bar(B_DRAIN), 0, Ctl{abort_flag, p.status});
+    }
+    __syncwarp();
+  } else {
+    // ===================================================== softmax warpgroups
+    const int s = warp >> 2;           // query tile of this warpgroup
+    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane; // row within the tile
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::S_COL0 + 128 * s;
+    const uint32_t tO = tmem + lane_off + C::O_COL0 + D * s;
+    int s_cnt = 0, u_it = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int u = unit_of_round<CAUSAL>(it, p);
+      if (u == -2) break;
+      if (u < 0) continue;
+      const Unit U = decode_unit<QST, CAUSAL>(u, p);
+      const int m_s = U.m0 + s * 128;
+      const int row = m_s + r;
+      const int ns = U.n_s[s];
+
+      float qd = 1.f, vref = 1.f;
+      const float* kd_row = nullptr;
+      const float* vd_row = nullptr;
+      if constexpr (DT == DT_E4M3) {
+        const int qb = m_s >> 7;
+        qd = (qb < p.nqb) ? __ldg(p.q_descale + ((long long)U.b * p.Hq + U.hq) * p.nqb + qb) : 1.f;
+        kd_row = p.k_descale + ((long long)U.b * p.Hkv + U.hk) * p.nkb;
+        vd_row = p.v_descale + ((long long)U.b * p.Hkv + U.hk) * p.nkb;
+        float vm = 0.f;
+        for (int t = lane; t < p.nkb; t += 32) vm = fmaxf(vm, __ldg(vd_row + t));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+        vref = vm > 0.f ? vm : 1.f;
+      }
+
+      float mi = -CUDART_INF_F;   // running max of the scaled logits (log2 units)
+      float li = 0.f;             // running sum of exp2(logit - mi)
+      for (int j = 0; j < ns; ++j) {
+        ok = warp_wait_bar(bar(B_SFULL + s), s_cnt & 1, ctl);
+        ++s_cnt;
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t sr[128];
+        ptx::tmem_ld_x128(tS, sr);
+        float sv[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
+
+        const int n0 = j * 128;
+        if ((n0 + 128 > p.Nk) || (CAUSAL && n0 + 127 > m_s)) {
+          int lim = p.Nk - n0;
+          if (CAUSAL) lim = min(lim, row - n0 + 1);
+#pragma unroll
+          for (int c = 0; c < 128; ++c) sv[c] = (c < lim) ? sv[c] : -CUDART_INF_F;
+        }
+
+        float cj = p.scale_log2;    // logit scale of this tile (log2 units)
+        float bias_extra = 0.f;     // FP8: exponent shift and V-block factor
+        float sum_scale = 1.f;      // FP8: converts the tile's row sum back to unit P
+        if constexpr (DT == DT_E4M3) {
+          const float kd = __ldg(kd_row + j);
+          const float rj = __ldg(vd_row + j) / vref;   // in (0, 1]
+          cj *= qd * kd;
+          bias_extra = C::PSHIFT + ptx::lg2(rj);
+          sum_scale = 1.f / rj;
+        }
+
+        // row max of this tile
+        float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, sv[c]);
+          mx1 = fmaxf(mx1, sv[c + 1]);
+          mx2 = fmaxf(mx2, sv[c + 2]);
+          mx3 = fmaxf(mx3, sv[c + 3]);
+        }
+        const float mj = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cj;
+        const float m_new = fmaxf(mi, mj);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          mi = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+        } else if (m_new > mi + C::TAU) {
+          // the new maximum exceeds the reference by more than 2^TAU:
+          // move the reference (merge rule of section 4.2) and rescale O, l
+          alpha = ptx::ex2(mi - m_new);
+          mi = m_new;
+          li *= alpha;
+          rescale = true;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int cb = 0; cb < D; cb += 32) {
+            uint32_t o32[32];
+            ptx::tmem_ld_x32(tO + cb, o32);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o32[c] = __float_as_uint(__uint_as_float(o32[c]) * alpha);
+            ptx::tmem_st_x32(tO + cb, o32);
+          }
+        }
+
+        // P = exp2(logit - reference), row sum, write P over S
+        const float bias = mi - bias_extra;
+        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          sv[c] = ptx::ex2(fmaf(sv[c], cj, -bias));
+          sv[c + 1] = ptx::ex2(fmaf(sv[c + 1], cj, -bias));
+          sv[c + 2] = ptx::ex2(fmaf(sv[c + 2], cj, -bias));
+          sv[c + 3] = ptx::ex2(fmaf(sv[c + 3], cj, -bias));
+          sum0 += sv[c];
+          sum1 += sv[c + 1];
+          sum2 += sv[c + 2];
+          sum3 += sv[c + 3];
+        }
+        li += ((sum0 + sum1) + (sum2 + sum3)) * sum_scale;
+        if constexpr (DT == DT_E4M3) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            pk[c] = ptx::pack_e4m3x4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
+          ptx::tmem_st_x32(tS, pk);
+        } else {
+          uint32_t pk[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            pk[c] = (DT == DT_BF16) ? ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1])
+                                    : ptx::pack_f16x2(sv[2 * c], sv[2 * c + 1]);
+          ptx::tmem_st_x64(tS, pk);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(B_PFULL + s));
+      }
+      if (!ok) break;
+
+      // ------------------------------------------------------------ epilogue
+      ok = warp_wait_bar(bar(B_OFULL + s), u_it & 1, ctl);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const float inv = (DT == DT_E4M3 ? vref : 1.f) / li;
+      const bool live = row < p.Nq;
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                       (((long long)U.b * p.Nq + row) * p.Hq + U.hq) * D;
+#pragma unroll 1
+      for (int cb = 0; cb < D; cb += 32) {
+        uint32_t o32[32];
+        ptx::tmem_ld_x32(tO + cb, o32);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a = __uint_as_float(o32[2 * c]) * inv;
+          const float b = __uint_as_float(o32[2 * c + 1]) * inv;
+          pk[c] = (DT == DT_F16) ? ptx::pack_f16x2(a, b) : ptx::pack_bf16x2(a, b);
+        }
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cb);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+      }
+      // l carries the factor 2^PSHIFT of the FP8 instance (0 otherwise)
+      if (live)
+        p.lse[((long long)U.b * p.Hq + U.hq) * p.Nq + row] =
+            (mi + ptx::lg2(li) - C::PSHIFT) * 0.6931471805599453f;
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(B_OEMPTY + s));
+      ++u_it;
+    }
+  }
+
+  // --------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == C::W_MMA) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,45 @@
+// fwd_launch.cuh - template launch helpers for the fused forward kernel;
+// included by the per-element-type translation units only.
+#pragma once
+
+#include "attn_fwd_kernel.cuh"
+#include "internal.h"
+
+namespace attn {
+
+template <int D, int DT, bool CAUSAL>
+int launch_fwd_instance(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                        const FwdParams& p, int grid, cudaStream_t stream) {
+  using C = FwdCfg<D, DT>;
+  auto kern = attn_fwd_kernel<D, DT, CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  kern<<<grid, C::NTHREADS, C::SMEM_BYTES, stream>>>(q, k, v, p);
+  note_launch();
+  return check_launch();
+}
+
+template <int DT>
+int launch_fwd_dt(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
+                  const CUtensorMap& v, const FwdParams& p, int grid, cudaStream_t stream) {
+  switch (d) {
+    case 64:
+      if constexpr (DT == DT_E4M3) {
+        return ATTN_ERR_UNSUPPORTED;
+      } else {
+        return causal ? launch_fwd_instance<64, DT, true>(q, k, v, p, grid, stream)
+                      : launch_fwd_instance<64, DT, false>(q, k, v, p, grid, stream);
+      }
+    case 128:
+      return causal ? launch_fwd_instance<128, DT, true>(q, k, v, p, grid, stream)
+                    : launch_fwd_instance<128, DT, false>(q, k, v, p, grid, stream);
+    case 256:
+      return causal ? launch_fwd_instance<256, DT, true>(q, k, v, p, grid, stream)
+                    : launch_fwd_instance<256, DT, false>(q, k, v, p, grid, stream);
+    default:
+      return ATTN_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace attn

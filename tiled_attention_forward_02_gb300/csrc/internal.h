@@ -1,0 +1,37 @@
+// internal.h - host-side declarations shared by the C-ABI layer (api.cu)
+// and the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+struct FwdParams;
+
+// counts one kernel launch (attn_launch_count)
+void note_launch();
+// turns the launch status into a return code, keeping the CUDA message
+int check_launch();
+// records a CUDA error text for attn_strerror and returns ATTN_ERR_CUDA
+int cuda_fail(cudaError_t e, const char* where);
+
+// fused forward launchers, one per element type; `grid` is the number of
+// persistent CTAs; d and causal select the template instance
+int launch_fwd_f16(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
+                   const CUtensorMap& v, const FwdParams& p, int grid, cudaStream_t stream);
+int launch_fwd_bf16(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
+                    const CUtensorMap& v, const FwdParams& p, int grid, cudaStream_t stream);
+int launch_fwd_e4m3(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
+                    const CUtensorMap& v, const FwdParams& p, int grid, cudaStream_t stream);
+
+// query tiles per work unit of the fused forward (tensor-memory budget)
+inline int fwd_q_tiles(int d) { return d == 256 ? 1 : 2; }
+
+int launch_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int N, int d,
+                    const int8_t* signs, int sign_group, int transpose_out, cudaStream_t stream);
+
+}  // namespace attn
