@@ -1,0 +1,157 @@
+"""GPU parity of the FP8 path: the prep kernel (per-block E4M3 quantisation,
+optional Hadamard transform) and the FP8 fused forward.
+
+* Prep without the transform: the quantised values are exact float32
+  quotients on both sides, so codes and descales must match the oracle bit
+  for bit (BSHD and transposed layouts).
+* Prep with the transform: the float32 butterfly and the oracle's float64
+  product may round the last bit differently, which can move a value across
+  an E4M3 rounding boundary.  Codes are checked against the exact value with
+  that slack; descales to float32 rounding.
+* FP8 forward: against the oracle run on its own dequantised FP8 inputs
+  (the kernel's arithmetic), and against the oracle on the original BF16
+  values (the truth): no error beyond the quantisation scheme's own, RMS
+  <= 5e-2 where the scheme can reach it (x10 outliers), and with the
+  transform no worse than without it on outlier-injected inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from oracle import fp8 as ofp8
+from parity import errors
+
+pytestmark = pytest.mark.gpu
+
+
+def _signs(G, d, dev="cuda"):
+    return synth.hadamard_signs(G, d, seed=0).to(dev)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [300, 4096])
+def test_prep_bit_exact_without_transform(gpu_lib, d, N):
+    B, H = 2, 3
+    x, _, _ = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=5,
+                                outlier_frac=1e-3)
+    codes, ds = gpu_lib.attn_prep_fp8(x.cuda())
+    codes_t, ds_t = gpu_lib.attn_prep_fp8(x.cuda(), transpose_out=True)
+    assert gpu_lib.get_status() == 0
+    oc, ods, _ = ofp8.prepare(x.float().numpy(), None, False)
+    np.testing.assert_array_equal(ds.cpu().numpy(), ods)
+    np.testing.assert_array_equal(ds_t.cpu().numpy(), ods)
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    npad = (N + 15) // 16 * 16
+    ct = codes_t.cpu().numpy()
+    assert ct.shape == (B, H, d, npad)
+    np.testing.assert_array_equal(ct[..., :N], oc.transpose(0, 2, 3, 1))
+    assert not ct[..., N:].any()   # padding keys are zero codes
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_prep_with_transform_matches_oracle(gpu_lib, d):
+    B, N, Hq, Hkv = 1, 520, 4, 2
+    x, _, _ = synth.attn_inputs(B, N, N, Hq, Hkv, d, dtype=torch.bfloat16, seed=6,
+                                outlier_frac=1e-3)
+    signs = _signs(Hkv, d)
+    codes, ds = gpu_lib.attn_prep_fp8(x.cuda(), signs=signs, sign_heads=Hkv)
+    assert gpu_lib.get_status() == 0
+    y64 = ofp8.incoherent_transform(x.double().numpy(), signs.cpu().numpy())
+    _, ods, y32 = ofp8.prepare(x.double().numpy(), signs.cpu().numpy(), True)
+    g_ds = ds.cpu().numpy()
+    np.testing.assert_allclose(g_ds, ods, rtol=4e-6, atol=0)
+    t = np.arange(N) // 128
+    q_exact = y64 / g_ds.astype(np.float64)[:, :, t].transpose(0, 2, 1)[..., None]
+    tol = 4e-6 * np.abs(q_exact) + 1e-30
+    lo, hi = ofp8.e4m3_encode(q_exact - tol), ofp8.e4m3_encode(q_exact + tol)
+    g = codes.cpu().numpy()
+    ok = (g == lo) | (g == hi)
+    assert ok.all(), np.argwhere(~ok)[:5]
+    # and almost all codes are the exact nearest-even code
+    assert np.mean(g != ofp8.e4m3_encode(q_exact)) < 1e-3
+
+
+def _fp8_forward(gpu_lib, q, k, v, causal, hadamard, Hkv):
+    d = q.shape[-1]
+    signs = _signs(Hkv, d) if hadamard else None
+    q8, qd = gpu_lib.attn_prep_fp8(q, signs=signs, sign_heads=Hkv if hadamard else None)
+    k8, kd = gpu_lib.attn_prep_fp8(k, signs=signs, sign_heads=Hkv if hadamard else None)
+    v8, vd = gpu_lib.attn_prep_fp8(v, transpose_out=True)
+    o, lse = gpu_lib.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=causal, hadamard=hadamard)
+    assert gpu_lib.get_status() == 0
+    return o, lse
+
+
+def _oracle_dequant(q, k, v, causal, hadamard, Hkv, rows=None):
+    """Oracle on its own FP8 quantisation of the same inputs (dequantised)."""
+    d = q.shape[-1]
+    sg = synth.hadamard_signs(Hkv, d, seed=0).numpy() if hadamard else None
+    deq = []
+    for t, had in ((q, hadamard), (k, hadamard), (v, False)):
+        c, ds, _ = ofp8.prepare(t.double().cpu().numpy(), sg, had)
+        deq.append(ofp8.dequantize(c, ds))
+    qd, kd, vd = deq
+    scale = 1 / math.sqrt(d)
+    if rows is None:
+        return oracle.attention_full(qd, kd, vd, causal=causal, scale=scale)
+    return oracle.attention_rows(qd[rows[:, 0], rows[:, 2], rows[:, 1]], kd, vd,
+                                 Hq=q.shape[2], causal=causal, scale=scale, rows=rows)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("hadamard", [False, True])
+@pytest.mark.parametrize("d", [128, 256])
+def test_fp8_forward_vs_dequantised_oracle(gpu_lib, causal, hadamard, d):
+    """Ragged multi-tile GQA case, every row: the kernel's arithmetic against
+    the oracle on the dequantised inputs.  The remaining error is the E4M3
+    rounding of P (relative 2^-4 at most) and the bf16 output."""
+    B, N, Hq, Hkv = 1, 700, 4, 2
+    q, k, v = synth.attn_inputs(B, N, N, Hq, Hkv, d, dtype=torch.bfloat16, seed=7,
+                                outlier_frac=1e-3, device="cuda")
+    o, lse = _fp8_forward(gpu_lib, q, k, v, causal, hadamard, Hkv)
+    o_ref, lse_ref = _oracle_dequant(q, k, v, causal, hadamard, Hkv)
+    e = errors(o, lse, o_ref, lse_ref)
+    assert e["nonfinite"] == 0, e
+    assert e["o_rel_rms"] <= 4e-2, e
+    assert e["lse_max_abs"] <= 2e-3, e
+
+
+@pytest.mark.parametrize("outlier_scale", [50.0, 10.0])
+def test_fp8_full_workload_accuracy_and_hadamard(gpu_lib, outlier_scale):
+    """B=4, H=16, N=4096, d=128, 0.1% of entries multiplied by `outlier_scale`.
+
+    Against the oracle on the original BF16 values (the truth), sampled rows:
+    * the GPU adds no error beyond the quantisation scheme itself: its RMS is
+      within 10 % of the RMS of the oracle run on its own E4M3 quantisation of
+      the same inputs;
+    * the Hadamard-processed run is no worse than plain FP8;
+    * at x10 outliers the RMS error is <= 5e-2.  At x50 the scheme's own error
+      (E4M3 rounding of Q and K when outliers make logits reach the hundreds)
+      is above that bound for any implementation of it, so the bound there is
+      the scheme's own error."""
+    B, N, H, d = 4, 4096, 16, 128
+    q, k, v = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=0,
+                                outlier_frac=1e-3, outlier_scale=outlier_scale, device="cuda")
+    rows = synth.sample_rows(B, H, N, per_head=32, seed=0)
+    idx = torch.as_tensor(rows, device="cuda")
+    q_rows = synth.raw_bits(q[idx[:, 0], idx[:, 2], idx[:, 1]])
+    o_ref, lse_ref = oracle.attention_rows(q_rows, synth.raw_bits(k), synth.raw_bits(v), Hq=H,
+                                           causal=False, scale=1 / math.sqrt(d), rows=rows,
+                                           elem=oracle.ELEM_BF16)
+    rms, rms_scheme = {}, {}
+    for had in (False, True):
+        o, lse = _fp8_forward(gpu_lib, q, k, v, False, had, H)
+        og = o[idx[:, 0], idx[:, 2], idx[:, 1]].double().cpu().numpy()
+        lg = lse[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
+        assert np.isfinite(og).all() and np.isfinite(lg).all()
+        rms[had] = math.sqrt(np.mean((og - o_ref) ** 2))
+        o_sch, _ = _oracle_dequant(q, k, v, False, had, H, rows=rows)
+        rms_scheme[had] = math.sqrt(np.mean((o_sch - o_ref) ** 2))
+        assert rms[had] <= 1.10 * rms_scheme[had] + 1e-3, (had, rms, rms_scheme)
+    assert rms[True] <= rms[False], rms
+    if outlier_scale <= 10.0:
+        assert rms[False] <= 5e-2 and rms[True] <= 5e-2, rms
