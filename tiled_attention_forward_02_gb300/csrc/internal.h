@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/attn.h"
+#include "attn.h"  // include/ is on the include path
 
 namespace attn {
 
