@@ -89,10 +89,17 @@ struct FwdCfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int S_COL0 = 0;                  // S_s at S_COL0 + 128 s
   static constexpr int O_COL0 = 128 * QST;          // O_s at O_COL0 + D s
-  static constexpr int NUM_WARPS = QST * 4 + 2;
+  // two query tiles: 2 softmax warpgroups + one warpgroup holding the MMA and
+  // TMA warps (and two idle warps) so registers can move between warpgroups
+  static constexpr int NUM_WARPS = (QST == 2) ? 12 : 6;
   static constexpr int NTHREADS = NUM_WARPS * 32;
   static constexpr int W_MMA = QST * 4;
   static constexpr int W_LOAD = QST * 4 + 1;
+  // register split (setmaxnreg) of the two-tile layout; the launch must give
+  // each thread at least LAUNCH_REGS so that the split fits in the block's pool
+  static constexpr int REG_SOFTMAX = 216;
+  static constexpr int REG_OTHER = 72;
+  static constexpr int LAUNCH_REGS = (2 * REG_SOFTMAX + REG_OTHER + 2) / 3;
   // softmax: lazy rescale threshold (log2 units) and exponent shift of P
   static constexpr float TAU = (DT == DT_E4M3) ? 2.0f : 8.0f;
   static constexpr float PSHIFT = (DT == DT_E4M3) ? 6.0f : 0.0f;
@@ -228,9 +235,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   constexpr int B_KVFULL = 3;                // [NSLOT] TMA K/V landed        (tx)
   constexpr int B_KVEMPTY = 3 + NSLOT;       // [NSLOT] GEMMs reading slot done (commit)
   constexpr int B_SFULL = 3 + 2 * NSLOT;     // [2]   S_s ready               (commit)
-  constexpr int B_PFULL = B_SFULL + 2;       // [2]   P_s written, O_s rescaled (128 arrivals)
+  constexpr int B_PFULL = B_SFULL + 2;       // [2]   P_s written, O_s rescaled (4 warp arrivals)
   constexpr int B_OFULL = B_PFULL + 2;       // [2]   last PV of unit done    (commit)
-  constexpr int B_OEMPTY = B_OFULL + 2;      // [2]   epilogue read O_s       (128 arrivals)
+  constexpr int B_OEMPTY = B_OFULL + 2;      // [2]   epilogue read O_s       (4 warp arrivals)
   constexpr int B_DRAIN = B_OEMPTY + 2;      // [1]   all MMAs of this CTA done (commit)
   constexpr int NBARS = B_DRAIN + 1;
   static_assert(NBARS * 8 + 16 <= C::SMEM_TAIL, "barrier table too large");
@@ -246,9 +253,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(bar(B_QFULL + s), 1);
       ptx::mbar_init(bar(B_SFULL + s), 1);
-      ptx::mbar_init(bar(B_PFULL + s), 128);
+      ptx::mbar_init(bar(B_PFULL + s), 4);   // one elected arrival per softmax warp
       ptx::mbar_init(bar(B_OFULL + s), 1);
-      ptx::mbar_init(bar(B_OEMPTY + s), 128);
+      ptx::mbar_init(bar(B_OEMPTY + s), 4);
     }
     ptx::mbar_init(bar(B_QEMPTY), 1);
     for (int i = 0; i < NSLOT; ++i) {
@@ -275,6 +282,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
 
   if (warp == C::W_LOAD) {
     // ===================================================== TMA producer
+    if constexpr (QST == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
     if (lane == 0) {
       int kv_it = 0, u_it = 0;
       bool ok = true;
@@ -335,6 +343,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     __syncwarp();
   } else if (warp == C::W_MMA) {
     // ===================================================== MMA issuer
+    if constexpr (QST == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
     if (lane == 0) {
       constexpr uint32_t fmt = (DT == DT_BF16) ? 1u : 0u;
       constexpr uint32_t idS = idesc_make(fmt, 128, 128, false);
@@ -351,21 +360,22 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         if (!ok) break;
         ptx::tc_fence_after();
         for (int j = 0; j <= U.n && ok; ++j) {
-          const int k_idx = kv_it + 2 * j;
-          const int v_idx = kv_it + 2 * j - 1;
+          const int k_idx = kv_it + 2 * j;       // ring index of K_j
+          const int v_idx = kv_it + 2 * j - 1;   // ring index of V_{j-1}
           const int kslot = k_idx % NSLOT;
           const int vslot = (v_idx + NSLOT) % NSLOT;
-          if (j < U.n) ok = wait_bar(bar(B_KVFULL + kslot), (k_idx / NSLOT) & 1, ctl);
-          if (ok && j >= 1) ok = wait_bar(bar(B_KVFULL + vslot), (v_idx / NSLOT) & 1, ctl);
-          if (!ok) break;
-          ptx::tc_fence_after();
+          bool k_ready = false, v_ready = false;
 #pragma unroll
           for (int s = 0; s < QST; ++s) {
             const uint32_t tS = tmem + C::S_COL0 + 128 * s;
             const uint32_t tO = tmem + C::O_COL0 + D * s;
             if (j >= 1 && j - 1 < U.n_s[s]) {
               // O_s += P_s V_{j-1}
-              ok = wait_bar(bar(B_PFULL + s), pv_cnt[s] & 1, ctl);
+              if (!v_ready) {
+                ok = wait_bar(bar(B_KVFULL + vslot), (v_idx / NSLOT) & 1, ctl);
+                v_ready = true;
+              }
+              if (ok) ok = wait_bar(bar(B_PFULL + s), pv_cnt[s] & 1, ctl);
               ++pv_cnt[s];
               if (ok && j == 1) ok = wait_bar(bar(B_OEMPTY + s), (u_it & 1) ^ 1, ctl);
               if (!ok) break;
@@ -384,9 +394,17 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                                   (j > 1 || kk > 0) ? 1u : 0u);
               }
               if (j - 1 == U.n_s[s] - 1) ptx::tc_commit(bar(B_OFULL + s));
+              // the last query tile always visits every key tile: it is the last reader
+              if (s == QST - 1) ptx::tc_commit(bar(B_KVEMPTY + vslot));
             }
             if (j < U.n_s[s]) {
               // S_s = Q_s K_j^T
+              if (!k_ready) {
+                ok = wait_bar(bar(B_KVFULL + kslot), (k_idx / NSLOT) & 1, ctl);
+                k_ready = true;
+                if (!ok) break;
+                ptx::tc_fence_after();
+              }
               const uint32_t qbase = sQ + s * C::QBYTES;
               const uint32_t kbase = sKV + kslot * C::KVBYTES;
               constexpr int KSTEPS = C::ROWB / 32;   // 32 bytes of K per MMA
@@ -401,11 +419,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                   ptx::mma_f16_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
               }
               ptx::tc_commit(bar(B_SFULL + s));
+              if (s == QST - 1) ptx::tc_commit(bar(B_KVEMPTY + kslot));
             }
           }
           if (!ok) break;
-          if (j < U.n) ptx::tc_commit(bar(B_KVEMPTY + kslot));
-          if (j >= 1) ptx::tc_commit(bar(B_KVEMPTY + vslot));
           if (j == U.n - 1) ptx::tc_commit(bar(B_QEMPTY));
         }
         kv_it += 2 * U.n;
@@ -416,8 +433,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       wait_bar(bar(B_DRAIN), 0, Ctl{abort_flag, p.status});
     }
     __syncwarp();
-  } else {
+  } else if (warp < QST * 4) {
     // ===================================================== softmax warpgroups
+    if constexpr (QST == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
     const int s = warp >> 2;           // query tile of this warpgroup
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane; // row within the tile
@@ -482,16 +500,18 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
           sum_scale = 1.f / rj;
         }
 
-        // row max of this tile
+        // row max of this tile (3-input max, four independent chains)
         float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, sv[c]);
-          mx1 = fmaxf(mx1, sv[c + 1]);
-          mx2 = fmaxf(mx2, sv[c + 2]);
-          mx3 = fmaxf(mx3, sv[c + 3]);
+        for (int c = 4; c < 124; c += 8) {
+          mx0 = ptx::max3(mx0, sv[c], sv[c + 1]);
+          mx1 = ptx::max3(mx1, sv[c + 2], sv[c + 3]);
+          mx2 = ptx::max3(mx2, sv[c + 4], sv[c + 5]);
+          mx3 = ptx::max3(mx3, sv[c + 6], sv[c + 7]);
         }
-        const float mj = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cj;
+        mx0 = ptx::max3(mx0, sv[124], sv[125]);
+        mx1 = ptx::max3(mx1, sv[126], sv[127]);
+        const float mj = ptx::max3(mx0, mx1, fmaxf(mx2, mx3)) * cj;
         const float m_new = fmaxf(mi, mj);
         float alpha = 1.f;
         bool rescale = false;
@@ -517,18 +537,19 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         }
 
         // P = exp2(logit - reference), row sum, write P over S
-        const float bias = mi - bias_extra;
+        const float nbias = bias_extra - mi;
         float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
         for (int c = 0; c < 128; c += 4) {
-          sv[c] = ptx::ex2(fmaf(sv[c], cj, -bias));
-          sv[c + 1] = ptx::ex2(fmaf(sv[c + 1], cj, -bias));
-          sv[c + 2] = ptx::ex2(fmaf(sv[c + 2], cj, -bias));
-          sv[c + 3] = ptx::ex2(fmaf(sv[c + 3], cj, -bias));
-          sum0 += sv[c];
-          sum1 += sv[c + 1];
-          sum2 += sv[c + 2];
-          sum3 += sv[c + 3];
+          float x0, x1, x2, x3;
+          ptx::fma2(x0, x1, sv[c], sv[c + 1], cj, cj, nbias, nbias);
+          ptx::fma2(x2, x3, sv[c + 2], sv[c + 3], cj, cj, nbias, nbias);
+          sv[c] = ptx::ex2(x0);
+          sv[c + 1] = ptx::ex2(x1);
+          sv[c + 2] = ptx::ex2(x2);
+          sv[c + 3] = ptx::ex2(x3);
+          ptx::add2(sum0, sum1, sv[c], sv[c + 1]);
+          ptx::add2(sum2, sum3, sv[c + 2], sv[c + 3]);
         }
         li += ((sum0 + sum1) + (sum2 + sum3)) * sum_scale;
         if constexpr (DT == DT_E4M3) {
@@ -547,7 +568,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(B_PFULL + s));
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(B_PFULL + s));
       }
       if (!ok) break;
 
@@ -582,9 +604,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         p.lse[((long long)U.b * p.Hq + U.hq) * p.Nq + row] =
             (mi + ptx::lg2(li) - C::PSHIFT) * 0.6931471805599453f;
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_OEMPTY + s));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(B_OEMPTY + s));
       ++u_it;
     }
+  } else {
+    // idle warps of the MMA/TMA warpgroup
+    if constexpr (QST == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
   }
 
   // --------------------------------------------------------------- teardown

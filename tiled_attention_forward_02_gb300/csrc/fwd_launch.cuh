@@ -12,6 +12,14 @@ int launch_fwd_instance(const CUtensorMap& q, const CUtensorMap& k, const CUtens
                         const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D, DT>;
   auto kern = attn_fwd_kernel<D, DT, CAUSAL>;
+  if constexpr (C::QST == 2) {
+    // the register split inside the kernel must fit in the block's pool,
+    // otherwise setmaxnreg.inc would wait forever: refuse to launch instead
+    cudaFuncAttributes fa;
+    cudaError_t ea = cudaFuncGetAttributes(&fa, kern);
+    if (ea != cudaSuccess) return cuda_fail(ea, "cudaFuncGetAttributes");
+    if (fa.numRegs < C::LAUNCH_REGS) return ATTN_ERR_DEVICE;
+  }
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
