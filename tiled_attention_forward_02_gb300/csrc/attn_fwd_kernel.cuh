@@ -191,11 +191,15 @@ struct Ctl {
   unsigned int* status;
 };
 
+// suspend-time hint of a waiting thread: waiters sleep in hardware instead of
+// spinning, so they do not take issue slots from the warps doing the work
+constexpr uint32_t kWaitSuspendNs = 200000;
+
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) return true;
     if (*ctl.abort_flag) return false;
     if (clock64() - t0 > kWaitBudgetCycles) {
       *ctl.abort_flag = 1;
@@ -470,7 +474,21 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
 
       float mi = -CUDART_INF_F;   // running max of the scaled logits (log2 units)
       float li = 0.f;             // running sum of exp2(logit - mi)
+      // FP8: descales of the next key tile are loaded one iteration ahead so
+      // their latency stays off the softmax critical path
+      float kd_next = 1.f, vd_next = 1.f;
+      if constexpr (DT == DT_E4M3) {
+        kd_next = __ldg(kd_row);
+        vd_next = __ldg(vd_row);
+      }
       for (int j = 0; j < ns; ++j) {
+        float kd_j = kd_next, vd_j = vd_next;
+        if constexpr (DT == DT_E4M3) {
+          if (j + 1 < ns) {
+            kd_next = __ldg(kd_row + j + 1);
+            vd_next = __ldg(vd_row + j + 1);
+          }
+        }
         ok = warp_wait_bar(bar(B_SFULL + s), s_cnt & 1, ctl);
         ++s_cnt;
         if (!ok) break;
@@ -493,25 +511,26 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         float bias_extra = 0.f;     // FP8: exponent shift and V-block factor
         float sum_scale = 1.f;      // FP8: converts the tile's row sum back to unit P
         if constexpr (DT == DT_E4M3) {
-          const float kd = __ldg(kd_row + j);
-          const float rj = __ldg(vd_row + j) / vref;   // in (0, 1]
-          cj *= qd * kd;
+          const float rj = vd_j / vref;   // in (0, 1]
+          cj *= qd * kd_j;
           bias_extra = C::PSHIFT + ptx::lg2(rj);
           sum_scale = 1.f / rj;
         }
 
-        // row max of this tile (3-input max, four independent chains)
-        float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+        // row max of this tile: 16 independent chains of 3-input max, then a tree
+        float mx[16];
 #pragma unroll
-        for (int c = 4; c < 124; c += 8) {
-          mx0 = ptx::max3(mx0, sv[c], sv[c + 1]);
-          mx1 = ptx::max3(mx1, sv[c + 2], sv[c + 3]);
-          mx2 = ptx::max3(mx2, sv[c + 4], sv[c + 5]);
-          mx3 = ptx::max3(mx3, sv[c + 6], sv[c + 7]);
+        for (int i = 0; i < 16; ++i) {
+          mx[i] = ptx::max3(sv[i], sv[i + 16], sv[i + 32]);
+          mx[i] = ptx::max3(mx[i], sv[i + 48], sv[i + 64]);
+          mx[i] = ptx::max3(mx[i], sv[i + 80], sv[i + 96]);
+          mx[i] = fmaxf(mx[i], sv[i + 112]);
         }
-        mx0 = ptx::max3(mx0, sv[124], sv[125]);
-        mx1 = ptx::max3(mx1, sv[126], sv[127]);
-        const float mj = ptx::max3(mx0, mx1, fmaxf(mx2, mx3)) * cj;
+        const float mxa = ptx::max3(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], mx[5]),
+                                    ptx::max3(mx[6], mx[7], mx[8]));
+        const float mxb = ptx::max3(ptx::max3(mx[9], mx[10], mx[11]),
+                                    ptx::max3(mx[12], mx[13], mx[14]), mx[15]);
+        const float mj = fmaxf(mxa, mxb) * cj;
         const float m_new = fmaxf(mi, mj);
         float alpha = 1.f;
         bool rescale = false;
@@ -536,36 +555,44 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
           }
         }
 
-        // P = exp2(logit - reference), row sum, write P over S
+        // P = exp2(logit - reference), row sum, write P over S in 32-column
+        // chunks as they are produced (the whole S row is already in registers)
         const float nbias = bias_extra - mi;
         float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          float x0, x1, x2, x3;
-          ptx::fma2(x0, x1, sv[c], sv[c + 1], cj, cj, nbias, nbias);
-          ptx::fma2(x2, x3, sv[c + 2], sv[c + 3], cj, cj, nbias, nbias);
-          sv[c] = ptx::ex2(x0);
-          sv[c + 1] = ptx::ex2(x1);
-          sv[c + 2] = ptx::ex2(x2);
-          sv[c + 3] = ptx::ex2(x3);
-          ptx::add2(sum0, sum1, sv[c], sv[c + 1]);
-          ptx::add2(sum2, sum3, sv[c + 2], sv[c + 3]);
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+          for (int c = 32 * k; c < 32 * k + 32; c += 4) {
+            float x0, x1, x2, x3;
+            ptx::fma2(x0, x1, sv[c], sv[c + 1], cj, cj, nbias, nbias);
+            ptx::fma2(x2, x3, sv[c + 2], sv[c + 3], cj, cj, nbias, nbias);
+            sv[c] = ptx::ex2(x0);
+            sv[c + 1] = ptx::ex2(x1);
+            sv[c + 2] = ptx::ex2(x2);
+            sv[c + 3] = ptx::ex2(x3);
+            ptx::add2(sum0, sum1, sv[c], sv[c + 1]);
+            ptx::add2(sum2, sum3, sv[c + 2], sv[c + 3]);
+          }
+          if constexpr (DT == DT_E4M3) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int e = 32 * k + 4 * c;
+              pk[c] = ptx::pack_e4m3x4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
+            }
+            ptx::tmem_st_x8(tS + 8 * k, pk);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int e = 32 * k + 2 * c;
+              pk[c] = (DT == DT_BF16) ? ptx::pack_bf16x2(sv[e], sv[e + 1])
+                                      : ptx::pack_f16x2(sv[e], sv[e + 1]);
+            }
+            ptx::tmem_st_x16(tS + 16 * k, pk);
+          }
         }
         li += ((sum0 + sum1) + (sum2 + sum3)) * sum_scale;
-        if constexpr (DT == DT_E4M3) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            pk[c] = ptx::pack_e4m3x4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
-          ptx::tmem_st_x32(tS, pk);
-        } else {
-          uint32_t pk[64];
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            pk[c] = (DT == DT_BF16) ? ptx::pack_bf16x2(sv[2 * c], sv[2 * c + 1])
-                                    : ptx::pack_f16x2(sv[2 * c], sv[2 * c + 1]);
-          ptx::tmem_st_x64(tS, pk);
-        }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
