@@ -41,6 +41,9 @@ WORKLOADS = {
     "bf16_causal_gqa_B1_Hq64_Hkv8_N131072_d128": (1, 64, 8, 131072, 131072, 128, True, "bf16"),
     "fp8_e4m3_B4_H16_N4096_d128": (4, 16, 16, 4096, 4096, 128, False, "fp8"),
     "fp8_e4m3_hadamard_B4_H16_N4096_d128": (4, 16, 16, 4096, 4096, 128, False, "fp8h"),
+    # one query per head against a long key cache: split key ranges + LSE merge
+    "bf16_decode_splitkv_B1_Hq64_Hkv8_Nq1_Nk131072_d128": (1, 64, 8, 1, 131072, 128, False,
+                                                          "decode"),
 }
 DEFAULT_WORKLOAD = "bf16_mha_B4_H16_N4096_d128"
 METRIC = "attention fwd TFLOPS (BF16, FP8) at 1 GB300 and % of dense tensor-core peak"
@@ -201,7 +204,7 @@ class OracleSampler:
         self.Hq, self.Nq, self.Nk, self.d, self.causal = Hq, Nq, Nk, d, causal
         # keys/values of batch element 0 only (the oracle decodes them in full per call)
         q, k, v = synth.attn_inputs(1, Nq, Nk, Hq, Hkv, d, dtype=torch.bfloat16, seed=0,
-                                    outlier_frac=1e-3 if kind != "bf16" else 0.0)
+                                    outlier_frac=1e-3 if kind.startswith("fp8") else 0.0)
         self.q, self.kb, self.vb = q, synth.raw_bits(k), synth.raw_bits(v)
         self.threads = oracle.default_threads()
         self.rng = np.random.default_rng(0)
@@ -282,7 +285,8 @@ def config_of(wl):
     return {"workload": wl, "B": B, "Hq": Hq, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d,
             "causal": causal, "scale": "1/sqrt(d)", "parallelism": "replicas",
             "l2": "inputs larger than L2 (Q+K+V+O > 129 MB), no flush between steps",
-            "inputs": "iid N(0,1) BSHD, seed 0" + (", 0.1% outliers x50" if kind != "bf16" else "")}
+            "inputs": "iid N(0,1) BSHD, seed 0" + (", 0.1% outliers x50"
+                                                  if kind.startswith("fp8") else "")}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -294,7 +298,7 @@ def make_step(wl, dev):
     from tiled_attention_forward_02_gb300 import attn
     B, Hq, Hkv, Nq, Nk, d, causal, kind = WORKLOADS[wl]
     scale = 1.0 / math.sqrt(d)
-    outl = 1e-3 if kind != "bf16" else 0.0
+    outl = 1e-3 if kind.startswith("fp8") else 0.0
     q, k, v = synth.attn_inputs(B, Nq, Nk, Hq, Hkv, d, dtype=torch.bfloat16, seed=0, device=dev,
                                 outlier_frac=outl)
     o = torch.empty_like(q)
@@ -306,6 +310,34 @@ def make_step(wl, dev):
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     meta["h2d"] = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     meta["d2h"] = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    if kind == "decode":
+        splits = attn.splitkv_default_splits(B, Hq, Nq, Nk, d)
+        ws = torch.empty(attn.splitkv_workspace_bytes(B, Hq, Nq, d, splits), dtype=torch.uint8,
+                         device=dev)
+
+        def step(kernel_events=None):
+            if kernel_events:
+                kernel_events[0].record()
+            attn.attn_fwd_splitkv(q, k, v, num_splits=splits, scale=scale, out=o, lse=lse,
+                                  workspace=ws)
+            if kernel_events:
+                kernel_events[1].record()
+
+        def e2e():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        rows = splits * B * Hq * Nq
+        # K and V once, Q, O, LSE, and the FP32 partial rows written and read back
+        meta["bytes"] = (2 * B * Nk * Hkv * d * 2 + 2 * B * Nq * Hq * d * 2 + B * Hq * Nq * 4
+                         + 2 * rows * (d + 1) * 4)
+        meta["launches_per_step"] = 2 if splits > 1 else 1
+        meta["kernel"] = f"attn_fwd_kernel<split> + splitkv_merge ({splits} splits)"
+        return step, e2e, meta
 
     if kind == "bf16":
         def step(kernel_events=None):
@@ -426,7 +458,14 @@ def gpu_arm(args, rank, world, local):
     avg_launch_ms = sum(per_launch_ms) / len(per_launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12   # dominant kernel alone
     kind = WORKLOADS[wl][7]
-    if kind == "bf16":
+    roof_unit, bound = "TFLOP/s", "tensor"
+    if kind == "decode":
+        # one query row per head: the path streams K and V once, HBM bound
+        achieved = meta["bytes"] / (avg_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        peak_note = f"HBM copy bandwidth, {peak_src}"
+        roof_unit, bound = "GB/s", "hbm"
+    elif kind == "bf16":
         peak = peaks["bf16_tflops"]
         peak_note = f"dense bf16, {peak_src} burst"
     else:
@@ -439,9 +478,9 @@ def gpu_arm(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if kind == "bf16" else "e4m3", "data": "synthetic",
+        "dtype": "e4m3" if kind.startswith("fp8") else "bf16", "data": "synthetic",
         "config": config_of(wl),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": roof_unit,
                      "frac": achieved / peak, "peak_source": peak_note,
                      "kernel": meta["kernel"],
                      "traffic": recorded_traffic(meta["kernel"], wl)},

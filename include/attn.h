@@ -46,6 +46,7 @@
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -137,6 +138,38 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q
                  const float* k_descale, const float* v_descale, void* o, float* lse, int B,
                  int Hq, int Hkv, int64_t Nq, int64_t Nk, int d, int causal, float scale,
                  int hadamard, void* stream);
+
+/*
+ * attn_fwd_splitkv - attn_fwd for long key sequences and few query rows
+ * (decode-like shapes), non-causal, FP16/BF16.  The key range of every query
+ * block is cut into `num_splits` consecutive ranges processed by different
+ * CTAs; each leaves its O / l and LSE in FP32 in `workspace`, and a second
+ * kernel combines them with the streaming-softmax merge rule of
+ * "FlashAttention（V3）深度解析" section 4.2 (m = max(m_a, m_b),
+ * z = z_a e^(m_a - m) + z_b e^(m_b - m)).  Same tensors, layouts and results
+ * as attn_fwd with causal = 0 (up to FP32 rounding of the merge).
+ *   num_splits  >= 1; more splits than 128-key tiles are reduced to one per
+ *               tile; an effective count of 1 runs attn_fwd's kernel alone
+ *   workspace   device buffer, 256-byte aligned, owned by the caller, at least
+ *               attn_splitkv_workspace_bytes(B, Hq, Nq, d, num_splits) bytes;
+ *               unused (may be NULL) when the effective count is 1.  Its
+ *               contents are scratch: overwritten by every call.
+ * Errors as attn_fwd; ATTN_ERR_INVALID_ARG also for num_splits < 1 or a
+ * workspace that is missing or too small.
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int64_t Nq, int64_t Nk, int d, int num_splits, float scale,
+                     int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* attn_splitkv_workspace_bytes - workspace attn_fwd_splitkv needs for these
+ * sizes (num_splits x B x Hq x Nq rows of d + 1 floats, plus alignment);
+ * 0 for invalid sizes.  No CUDA call. */
+size_t attn_splitkv_workspace_bytes(int B, int Hq, int64_t Nq, int d, int num_splits);
+
+/* attn_splitkv_default_splits - a split count that gives one wave of CTAs on
+ * the current device for these sizes (at least 1, at most one per key tile,
+ * at most 256).  Performs the one-time device set-up if needed. */
+int attn_splitkv_default_splits(int B, int Hq, int64_t Nq, int64_t Nk, int d);
 
 /*
  * attn_get_status - synchronise `stream`, then read and clear the device

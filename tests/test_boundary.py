@@ -117,3 +117,21 @@ def test_python_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         attn.attn_fwd(q, q, q)
+
+
+def test_splitkv_workspace_size_and_host_checks(lib):
+    # splits x B x Hq x Nq rows of d floats (padded to 256 bytes), then one float per row
+    assert lib.attn_splitkv_workspace_bytes(1, 2, 4, 128, 8) == 64 * 128 * 4 + 64 * 4
+    assert lib.attn_splitkv_workspace_bytes(1, 2, 3, 64, 1) == 1536 + 24
+    assert lib.attn_splitkv_workspace_bytes(1, 2, 4, 128, 0) == 0
+    args = [A, A, A, A, A, 1, 2, 2, 4, 4096, 128, 4, 0.1, 1, A, 1 << 20, None]
+    bad = list(args); bad[11] = 0
+    assert lib.attn_fwd_splitkv(*bad) == attn.ERR_INVALID_ARG        # no split
+    bad = list(args); bad[10] = 96
+    assert lib.attn_fwd_splitkv(*bad) == attn.ERR_UNSUPPORTED
+    bad = list(args); bad[14] = None
+    assert lib.attn_fwd_splitkv(*bad) == attn.ERR_INVALID_ARG        # workspace missing
+    bad = list(args); bad[15] = 1024
+    assert lib.attn_fwd_splitkv(*bad) == attn.ERR_INVALID_ARG        # workspace too small
+    bad = list(args); bad[14] = A + 64
+    assert lib.attn_fwd_splitkv(*bad) == attn.ERR_MISALIGNED

@@ -23,7 +23,8 @@ ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED = -1, -2, -3
 ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = -4, -5, -6
 
 EXPORTS = ("attn_fwd", "attn_prep_fp8", "attn_fwd_fp8", "attn_get_status", "attn_strerror",
-           "attn_launch_count")
+           "attn_launch_count", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
+           "attn_splitkv_default_splits")
 
 _lib = None
 
@@ -57,6 +58,13 @@ def load():
     lib.attn_strerror.argtypes = [i32]
     lib.attn_launch_count.restype = i64
     lib.attn_launch_count.argtypes = []
+    lib.attn_fwd_splitkv.restype = i32
+    lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32, f32,
+                                     i32, vp, ctypes.c_size_t, vp]
+    lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_splitkv_workspace_bytes.argtypes = [i32, i32, i64, i32, i32]
+    lib.attn_splitkv_default_splits.restype = i32
+    lib.attn_splitkv_default_splits.argtypes = [i32, i32, i64, i64, i32]
     _lib = lib
     return lib
 
@@ -120,6 +128,44 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                          int(bool(causal)), float(scale), dt, _stream(stream))
     _check(rc, "attn_fwd")
+    return out, lse
+
+
+def splitkv_workspace_bytes(B, Hq, Nq, d, num_splits) -> int:
+    return int(load().attn_splitkv_workspace_bytes(B, Hq, Nq, d, num_splits))
+
+
+def splitkv_default_splits(B, Hq, Nq, Nk, d) -> int:
+    return int(load().attn_splitkv_default_splits(B, Hq, Nq, Nk, d))
+
+
+def attn_fwd_splitkv(q, k, v, num_splits: int | None = None, scale: float | None = None,
+                     out=None, lse=None, workspace=None, stream=None):
+    """Non-causal attention with the key range split over several CTAs and an
+    LSE merge (decode-like shapes).  Same arguments and results as attn_fwd
+    with causal=False; `workspace` is a uint8 CUDA tensor of at least
+    splitkv_workspace_bytes(...) bytes (allocated here if None)."""
+    _need_cuda(q, k, v)
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must all be float16 or all bfloat16")
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    if num_splits is None:
+        num_splits = splitkv_default_splits(B, Hq, Nq, Nk, d)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    nbytes = splitkv_workspace_bytes(B, Hq, Nq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F16
+    rc = load().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq,
+                                 Nk, d, int(num_splits), float(scale), dt, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_fwd_splitkv")
     return out, lse
 
 

@@ -119,10 +119,10 @@ int check_common(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int causal, flo
 }
 
 int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, float scale,
-                const DeviceState& st, int* grid) {
+                const DeviceState& st, int* grid, int n_splits = 1, int split_tiles = 0) {
   const int qst = fwd_q_tiles(d);
   const int64_t n_mb = (Nq + qst * 128 - 1) / (qst * 128);
-  const int64_t units = (int64_t)B * Hq * n_mb;
+  const int64_t units = (int64_t)B * Hq * n_mb * n_splits;
   if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   p.B = B;
   p.Hq = Hq;
@@ -137,6 +137,9 @@ int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t
   p.nkb = (int)((Nk + 127) / 128);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st.status;
+  p.active_stages = (Nq <= 128) ? 1 : qst;   // the second query tile would hold only padding
+  p.n_splits = n_splits;
+  p.split_tiles = split_tiles > 0 ? split_tiles : p.n_kv_tiles;
   *grid = (int)(units < st.sm_count ? units : st.sm_count);
   return ATTN_OK;
 }
@@ -246,6 +249,96 @@ extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int
   const int group = signs ? H / sign_heads : 1;
   return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, transpose_out,
                          static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+// key tiles per split and the number of non-empty splits for a request
+void split_layout(int64_t Nk, int num_splits, int* split_tiles, int* eff_splits) {
+  const int tiles = (int)((Nk + 127) / 128);
+  int n = num_splits < 1 ? 1 : (num_splits > tiles ? tiles : num_splits);
+  const int per = (tiles + n - 1) / n;
+  *split_tiles = per;
+  *eff_splits = (tiles + per - 1) / per;
+}
+
+int64_t splitkv_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, int64_t splits) {
+  const int64_t rows = splits * B * Hq * Nq;
+  const int64_t o_bytes = (rows * d * 4 + 255) / 256 * 256;   // LSE part starts 256-aligned
+  return o_bytes + rows * 4;
+}
+}  // namespace
+
+extern "C" size_t attn_splitkv_workspace_bytes(int B, int Hq, int64_t Nq, int d, int num_splits) {
+  if (B < 0 || Hq < 1 || Nq < 0 || d < 1 || num_splits < 1) return 0;
+  return (size_t)splitkv_bytes(B, Hq, Nq, d, num_splits);
+}
+
+extern "C" int attn_splitkv_default_splits(int B, int Hq, int64_t Nq, int64_t Nk, int d) {
+  if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1) return 1;
+  DeviceState* st = nullptr;
+  if (device_state(&st) != ATTN_OK) return 1;
+  const int qst = fwd_q_tiles(d);
+  const int64_t units = (int64_t)B * Hq * ((Nq + qst * 128 - 1) / (qst * 128));
+  const int64_t tiles = (Nk + 127) / 128;
+  int64_t n = (st->sm_count + units - 1) / units;   // enough units for one wave
+  if (n > tiles) n = tiles;
+  if (n > 256) n = 256;
+  return (int)(n < 1 ? 1 : n);
+}
+
+extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d,
+                                int num_splits, float scale, int dtype, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  int rc = check_common(B, Hq, Hkv, Nq, Nk, 0, scale);
+  if (rc < 0) return rc;
+  if (num_splits < 1) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (rc == 1) return ATTN_OK;  // empty problem
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 128) || !aligned(k, 128) || !aligned(v, 128) || !aligned(o, 128) ||
+      !aligned(lse, 16))
+    return ATTN_ERR_MISALIGNED;
+  int split_tiles = 0, eff = 1;
+  split_layout(Nk, num_splits, &split_tiles, &eff);
+  if (eff > 1) {
+    if (!workspace) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return ATTN_ERR_MISALIGNED;
+    if ((int64_t)workspace_bytes < splitkv_bytes(B, Hq, Nq, d, eff)) return ATTN_ERR_INVALID_ARG;
+  }
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  const CUtensorMapDataType tdt =
+      dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap mq, mk, mv;
+  if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64)) ||
+      (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64)) ||
+      (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64)))
+    return rc;
+  FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  int grid = 0;
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid, eff, split_tiles)) != ATTN_OK)
+    return rc;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (eff > 1) {
+    const int64_t rows = (int64_t)eff * B * Hq * Nq;
+    o_part = static_cast<float*>(workspace);
+    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        (rows * d * 4 + 255) / 256 * 256);
+  }
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int mode = eff > 1 ? 2 : 0;   // 2: split instance writing partial results
+  rc = dtype == ATTN_BF16 ? launch_fwd_bf16(d, mode, mq, mk, mv, p, grid, s)
+                          : launch_fwd_f16(d, mode, mq, mk, mv, p, grid, s);
+  if (rc != ATTN_OK || eff == 1) return rc;
+  return launch_splitkv_merge(o_part, lse_part, o, lse, eff, B, Hq, (int)Nq, d, dtype,
+                              st->sm_count, s);
 }
 
 extern "C" int attn_get_status(void* stream) {

@@ -67,6 +67,13 @@ struct FwdParams {
   int n_units;             // B * Hq * n_mblocks
   int nqb, nkb;            // descale blocks per head
   float scale_log2;        // scale * log2(e)
+  int active_stages;       // query tiles per unit that hold rows (1 when Nq <= 128)
+  // split key ranges (non-causal only): unit = (head, row block, split); a
+  // split covers split_tiles key tiles and writes FP32 partial results
+  int n_splits;            // 1: no split, results go to o / lse
+  int split_tiles;         // key tiles per split
+  float* o_part;           // [n_splits, B, Hq, Nq, D] O / l of the split (n_splits > 1)
+  float* lse_part;         // [n_splits, B, Hq, Nq] natural-log LSE of the split
 };
 
 template <int D, int DT>
@@ -137,37 +144,49 @@ __host__ __device__ constexpr uint32_t idesc_make(uint32_t fmt, int M, int N, bo
 // ----------------------------------------------------------------- scheduling
 struct Unit {
   int b, hq, hk, m0;
+  int j0;       // first key tile of the unit's key range
+  int sp;       // split index
   int n_s[2];   // key tiles each query tile visits
   int n;        // max over the tiles
 };
 
-template <int QST, bool CAUSAL>
+template <int QST, bool CAUSAL, bool SPLIT>
 __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
   Unit U;
   const int BH = p.B * p.Hq;
   int mb, bh;
+  U.sp = 0;
   if (CAUSAL) {  // heaviest row blocks first, heads interleaved
     mb = p.n_mblocks - 1 - u / BH;
     bh = u % BH;
-  } else {       // head-major: concurrent CTAs share one head's K/V in L2
-    bh = u / p.n_mblocks;
-    mb = u % p.n_mblocks;
+  } else {       // head-major (then row block, then split): concurrent CTAs share
+                 // one head's K/V in L2, or stream disjoint ranges of it
+    int v = u;
+    if (SPLIT) {
+      U.sp = u % p.n_splits;
+      v = u / p.n_splits;
+    }
+    bh = v / p.n_mblocks;
+    mb = v % p.n_mblocks;
   }
   U.b = bh / p.Hq;
   U.hq = bh % p.Hq;
   U.hk = U.hq / p.group;
   U.m0 = mb * QST * 128;
+  U.j0 = SPLIT ? U.sp * p.split_tiles : 0;
   U.n = 0;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    int n = p.n_kv_tiles;
+    int n = p.n_kv_tiles - U.j0;
+    if (SPLIT && p.split_tiles < n) n = p.split_tiles;
     if (CAUSAL) {
       const int last_row = U.m0 + s * 128 + 127;  // top-left aligned mask
       const int need = last_row / 128 + 1;
       n = need < n ? need : n;
     }
-    U.n_s[s] = (s < QST) ? n : 0;
-    if (s < QST && n > U.n) U.n = n;
+    const bool active = s < QST && (!SPLIT || s < p.active_stages);
+    U.n_s[s] = active ? n : 0;
+    if (active && n > U.n) U.n = n;
   }
   return U;
 }
@@ -217,7 +236,7 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, con
 }
 
 // --------------------------------------------------------------------- kernel
-template <int D, int DT, bool CAUSAL>
+template <int D, int DT, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -252,6 +271,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Ctl ctl{abort_flag, p.status};
+  // query tiles that hold rows: only the split (decode) instances skip an
+  // all-padding second tile; the others keep the count a compile-time constant
+  const int n_active = SPLIT ? (QST < p.active_stages ? QST : p.active_stages) : QST;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -295,10 +317,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         const int u = unit_of_round<CAUSAL>(it, p);
         if (u == -2) break;
         if (u < 0) continue;
-        const Unit U = decode_unit<QST, CAUSAL>(u, p);
+        const Unit U = decode_unit<QST, CAUSAL, SPLIT>(u, p);
         ok = wait_bar(bar(B_QEMPTY), (u_it & 1) ^ 1, ctl);
         if (!ok) break;
-        for (int s = 0; s < QST; ++s) {
+        for (int s = 0; s < n_active; ++s) {
           ptx::mbar_arrive_expect_tx(bar(B_QFULL + s), C::QBYTES);
           for (int ch = 0; ch < C::NCH; ++ch)
             ptx::tma_load_4d(sQ + s * C::QBYTES + ch * C::CHUNK_BYTES, &tmQ, bar(B_QFULL + s),
@@ -313,8 +335,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
             ptx::mbar_arrive_expect_tx(bar(B_KVFULL + slot), C::KVBYTES);
             for (int ch = 0; ch < C::NCH; ++ch)
               ptx::tma_load_4d_hint(sKV + slot * C::KVBYTES + ch * C::CHUNK_BYTES, &tmK,
-                                    bar(B_KVFULL + slot), ch * C::CH_ELEMS, U.hk, j * 128, U.b,
-                                    pol_kv);
+                                    bar(B_KVFULL + slot), ch * C::CH_ELEMS, U.hk,
+                                    (U.j0 + j) * 128, U.b, pol_kv);
             ++kv_it;
           }
           // V_j (FP8: one box of the transposed tensor, D rows x 128 keys)
@@ -324,13 +346,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
             if (!ok) break;
             ptx::mbar_arrive_expect_tx(bar(B_KVFULL + slot), C::KVBYTES);
             if constexpr (DT == DT_E4M3) {
-              ptx::tma_load_4d_hint(sKV + slot * C::KVBYTES, &tmV, bar(B_KVFULL + slot), j * 128,
-                                    0, U.hk, U.b, pol_kv);
+              ptx::tma_load_4d_hint(sKV + slot * C::KVBYTES, &tmV, bar(B_KVFULL + slot),
+                                    (U.j0 + j) * 128, 0, U.hk, U.b, pol_kv);
             } else {
               for (int ch = 0; ch < C::NCH; ++ch)
                 ptx::tma_load_4d_hint(sKV + slot * C::KVBYTES + ch * C::CHUNK_BYTES, &tmV,
-                                      bar(B_KVFULL + slot), ch * C::CH_ELEMS, U.hk, j * 128, U.b,
-                                      pol_kv);
+                                      bar(B_KVFULL + slot), ch * C::CH_ELEMS, U.hk,
+                                      (U.j0 + j) * 128, U.b, pol_kv);
             }
             ++kv_it;
           }
@@ -342,7 +364,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       for (int t = kv_it - pending; t < kv_it; ++t)
         wait_bar(bar(B_KVFULL + t % NSLOT), (t / NSLOT) & 1, Ctl{abort_flag, p.status});
       if (u_it > 0)
-        for (int s = 0; s < QST; ++s) wait_bar(bar(B_QFULL + s), (u_it - 1) & 1, ctl);
+        for (int s = 0; s < n_active; ++s)
+          wait_bar(bar(B_QFULL + s), (u_it - 1) & 1, ctl);
     }
     __syncwarp();
   } else if (warp == C::W_MMA) {
@@ -359,8 +382,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         const int u = unit_of_round<CAUSAL>(it, p);
         if (u == -2) break;
         if (u < 0) continue;
-        const Unit U = decode_unit<QST, CAUSAL>(u, p);
-        for (int s = 0; s < QST && ok; ++s) ok = wait_bar(bar(B_QFULL + s), u_it & 1, ctl);
+        const Unit U = decode_unit<QST, CAUSAL, SPLIT>(u, p);
+        for (int s = 0; s < n_active && ok; ++s)
+          ok = wait_bar(bar(B_QFULL + s), u_it & 1, ctl);
+        const int s_last = n_active - 1;
         if (!ok) break;
         ptx::tc_fence_after();
         for (int j = 0; j <= U.n && ok; ++j) {
@@ -398,8 +423,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                                   (j > 1 || kk > 0) ? 1u : 0u);
               }
               if (j - 1 == U.n_s[s] - 1) ptx::tc_commit(bar(B_OFULL + s));
-              // the last query tile always visits every key tile: it is the last reader
-              if (s == QST - 1) ptx::tc_commit(bar(B_KVEMPTY + vslot));
+              // the last active query tile visits every key tile: it is the last reader
+              if (s == s_last) ptx::tc_commit(bar(B_KVEMPTY + vslot));
             }
             if (j < U.n_s[s]) {
               // S_s = Q_s K_j^T
@@ -423,7 +448,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                   ptx::mma_f16_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
               }
               ptx::tc_commit(bar(B_SFULL + s));
-              if (s == QST - 1) ptx::tc_commit(bar(B_KVEMPTY + kslot));
+              if (s == s_last) ptx::tc_commit(bar(B_KVEMPTY + kslot));
             }
           }
           if (!ok) break;
@@ -448,11 +473,12 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     const uint32_t tO = tmem + lane_off + C::O_COL0 + D * s;
     int s_cnt = 0, u_it = 0;
     bool ok = true;
-    for (int it = 0; ok; ++it) {
+    // a query tile that holds no rows in this launch (Nq <= 128) does nothing
+    for (int it = 0; ok && s < n_active; ++it) {
       const int u = unit_of_round<CAUSAL>(it, p);
       if (u == -2) break;
       if (u < 0) continue;
-      const Unit U = decode_unit<QST, CAUSAL>(u, p);
+      const Unit U = decode_unit<QST, CAUSAL, SPLIT>(u, p);
       const int m_s = U.m0 + s * 128;
       const int row = m_s + r;
       const int ns = U.n_s[s];
@@ -476,19 +502,26 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       float li = 0.f;             // running sum of exp2(logit - mi)
       // FP8: descales of the next key tile are loaded one iteration ahead so
       // their latency stays off the softmax critical path
+      // FP8: the per-tile factors of tile j (logit scale, exponent bias, sum
+      // scale) are computed at the end of tile j-1, from descales loaded a
+      // tile earlier still, so neither the loads nor the divisions sit on
+      // the softmax critical path
+      float cj_cur = p.scale_log2, bias_cur = 0.f, ssc_cur = 1.f;
       float kd_next = 1.f, vd_next = 1.f;
+      auto fp8_factors = [&](float kd, float vd, float& cjo, float& bo, float& sso) {
+        const float rj = vd / vref;   // in (0, 1]
+        cjo = p.scale_log2 * qd * kd;
+        bo = C::PSHIFT + ptx::lg2(rj);
+        sso = 1.f / rj;
+      };
       if constexpr (DT == DT_E4M3) {
-        kd_next = __ldg(kd_row);
-        vd_next = __ldg(vd_row);
+        fp8_factors(__ldg(kd_row + U.j0), __ldg(vd_row + U.j0), cj_cur, bias_cur, ssc_cur);
+        if (ns > 1) {
+          kd_next = __ldg(kd_row + U.j0 + 1);
+          vd_next = __ldg(vd_row + U.j0 + 1);
+        }
       }
       for (int j = 0; j < ns; ++j) {
-        float kd_j = kd_next, vd_j = vd_next;
-        if constexpr (DT == DT_E4M3) {
-          if (j + 1 < ns) {
-            kd_next = __ldg(kd_row + j + 1);
-            vd_next = __ldg(vd_row + j + 1);
-          }
-        }
         ok = warp_wait_bar(bar(B_SFULL + s), s_cnt & 1, ctl);
         ++s_cnt;
         if (!ok) break;
@@ -499,7 +532,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
 
-        const int n0 = j * 128;
+        const int n0 = (U.j0 + j) * 128;
         if ((n0 + 128 > p.Nk) || (CAUSAL && n0 + 127 > m_s)) {
           int lim = p.Nk - n0;
           if (CAUSAL) lim = min(lim, row - n0 + 1);
@@ -507,15 +540,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
           for (int c = 0; c < 128; ++c) sv[c] = (c < lim) ? sv[c] : -CUDART_INF_F;
         }
 
-        float cj = p.scale_log2;    // logit scale of this tile (log2 units)
-        float bias_extra = 0.f;     // FP8: exponent shift and V-block factor
-        float sum_scale = 1.f;      // FP8: converts the tile's row sum back to unit P
-        if constexpr (DT == DT_E4M3) {
-          const float rj = vd_j / vref;   // in (0, 1]
-          cj *= qd * kd_j;
-          bias_extra = C::PSHIFT + ptx::lg2(rj);
-          sum_scale = 1.f / rj;
-        }
+        const float cj = cj_cur;           // logit scale of this tile (log2 units)
+        const float bias_extra = bias_cur; // FP8: exponent shift and V-block factor
+        const float sum_scale = ssc_cur;   // FP8: converts the tile's row sum back to unit P
 
         // row max of this tile: 16 independent chains of 3-input max, then a tree
         float mx[16];
@@ -597,6 +624,15 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(B_PFULL + s));
+        if constexpr (DT == DT_E4M3) {
+          if (j + 1 < ns) {
+            fp8_factors(kd_next, vd_next, cj_cur, bias_cur, ssc_cur);
+            if (j + 2 < ns) {
+              kd_next = __ldg(kd_row + U.j0 + j + 2);
+              vd_next = __ldg(vd_row + U.j0 + j + 2);
+            }
+          }
+        }
       }
       if (!ok) break;
 
@@ -606,30 +642,49 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       ptx::tc_fence_after();
       const float inv = (DT == DT_E4M3 ? vref : 1.f) / li;
       const bool live = row < p.Nq;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                       (((long long)U.b * p.Nq + row) * p.Hq + U.hq) * D;
-#pragma unroll 1
-      for (int cb = 0; cb < D; cb += 32) {
-        uint32_t o32[32];
-        ptx::tmem_ld_x32(tO + cb, o32);
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a = __uint_as_float(o32[2 * c]) * inv;
-          const float b = __uint_as_float(o32[2 * c + 1]) * inv;
-          pk[c] = (DT == DT_F16) ? ptx::pack_f16x2(a, b) : ptx::pack_bf16x2(a, b);
-        }
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cb);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        }
-      }
       // l carries the factor 2^PSHIFT of the FP8 instance (0 otherwise)
-      if (live)
-        p.lse[((long long)U.b * p.Hq + U.hq) * p.Nq + row] =
-            (mi + ptx::lg2(li) - C::PSHIFT) * 0.6931471805599453f;
+      const float lse_row = (mi + ptx::lg2(li) - C::PSHIFT) * 0.6931471805599453f;
+      if constexpr (SPLIT) {
+        // partial result of this key range: FP32 O / l and its LSE
+        const long long prow = (((long long)U.sp * p.B + U.b) * p.Hq + U.hq) * p.Nq + row;
+        float* dst = p.o_part + prow * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 32) {
+          uint32_t o32[32];
+          ptx::tmem_ld_x32(tO + cb, o32);
+          if (live) {
+            float4* d4 = reinterpret_cast<float4*>(dst + cb);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              d4[c] = make_float4(__uint_as_float(o32[4 * c]) * inv, __uint_as_float(o32[4 * c + 1]) * inv,
+                                  __uint_as_float(o32[4 * c + 2]) * inv,
+                                  __uint_as_float(o32[4 * c + 3]) * inv);
+          }
+        }
+        if (live) p.lse_part[prow] = lse_row;
+      } else {
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                         (((long long)U.b * p.Nq + row) * p.Hq + U.hq) * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D; cb += 32) {
+          uint32_t o32[32];
+          ptx::tmem_ld_x32(tO + cb, o32);
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float a = __uint_as_float(o32[2 * c]) * inv;
+            const float b = __uint_as_float(o32[2 * c + 1]) * inv;
+            pk[c] = (DT == DT_F16) ? ptx::pack_f16x2(a, b) : ptx::pack_bf16x2(a, b);
+          }
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cb);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          }
+        }
+        if (live) p.lse[((long long)U.b * p.Hq + U.hq) * p.Nq + row] = lse_row;
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(B_OEMPTY + s));

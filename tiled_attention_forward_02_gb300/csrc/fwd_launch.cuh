@@ -7,11 +7,11 @@
 
 namespace attn {
 
-template <int D, int DT, bool CAUSAL>
+template <int D, int DT, bool CAUSAL, bool SPLIT>
 int launch_fwd_instance(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                         const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D, DT>;
-  auto kern = attn_fwd_kernel<D, DT, CAUSAL>;
+  auto kern = attn_fwd_kernel<D, DT, CAUSAL, SPLIT>;
   if constexpr (C::QST == 2) {
     // the register split inside the kernel must fit in the block's pool,
     // otherwise setmaxnreg.inc would wait forever: refuse to launch instead
@@ -28,25 +28,29 @@ int launch_fwd_instance(const CUtensorMap& q, const CUtensorMap& k, const CUtens
   return check_launch();
 }
 
+// causal: 0 or 1; 2 = non-causal with the key range split (FP32 partial results)
+template <int DT, int D>
+int launch_fwd_d(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                 const FwdParams& p, int grid, cudaStream_t stream) {
+  switch (causal) {
+    case 0: return launch_fwd_instance<D, DT, false, false>(q, k, v, p, grid, stream);
+    case 1: return launch_fwd_instance<D, DT, true, false>(q, k, v, p, grid, stream);
+    default:
+      if constexpr (DT == DT_E4M3) return ATTN_ERR_UNSUPPORTED;
+      else return launch_fwd_instance<D, DT, false, true>(q, k, v, p, grid, stream);
+  }
+}
+
 template <int DT>
 int launch_fwd_dt(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
                   const CUtensorMap& v, const FwdParams& p, int grid, cudaStream_t stream) {
   switch (d) {
     case 64:
-      if constexpr (DT == DT_E4M3) {
-        return ATTN_ERR_UNSUPPORTED;
-      } else {
-        return causal ? launch_fwd_instance<64, DT, true>(q, k, v, p, grid, stream)
-                      : launch_fwd_instance<64, DT, false>(q, k, v, p, grid, stream);
-      }
-    case 128:
-      return causal ? launch_fwd_instance<128, DT, true>(q, k, v, p, grid, stream)
-                    : launch_fwd_instance<128, DT, false>(q, k, v, p, grid, stream);
-    case 256:
-      return causal ? launch_fwd_instance<256, DT, true>(q, k, v, p, grid, stream)
-                    : launch_fwd_instance<256, DT, false>(q, k, v, p, grid, stream);
-    default:
-      return ATTN_ERR_UNSUPPORTED;
+      if constexpr (DT == DT_E4M3) return ATTN_ERR_UNSUPPORTED;
+      else return launch_fwd_d<DT, 64>(causal, q, k, v, p, grid, stream);
+    case 128: return launch_fwd_d<DT, 128>(causal, q, k, v, p, grid, stream);
+    case 256: return launch_fwd_d<DT, 256>(causal, q, k, v, p, grid, stream);
+    default: return ATTN_ERR_UNSUPPORTED;
   }
 }
 

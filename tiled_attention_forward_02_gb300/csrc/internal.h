@@ -20,7 +20,8 @@ int check_launch();
 int cuda_fail(cudaError_t e, const char* where);
 
 // fused forward launchers, one per element type; `grid` is the number of
-// persistent CTAs; d and causal select the template instance
+// persistent CTAs; d and causal select the template instance (causal 2:
+// non-causal with a split key range, writing FP32 partial results)
 int launch_fwd_f16(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
                    const CUtensorMap& v, const FwdParams& p, int grid, cudaStream_t stream);
 int launch_fwd_bf16(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
@@ -30,6 +31,11 @@ int launch_fwd_e4m3(int d, int causal, const CUtensorMap& q, const CUtensorMap& 
 
 // query tiles per work unit of the fused forward (tensor-memory budget)
 inline int fwd_q_tiles(int d) { return d == 256 ? 1 : 2; }
+
+// combines split partial results (O / l per split, LSE per split) into o, lse
+int launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                         int n_splits, int B, int Hq, int Nq, int d, int dtype, int sm_count,
+                         cudaStream_t stream);
 
 int launch_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int N, int d,
                     const int8_t* signs, int sign_group, int transpose_out, cudaStream_t stream);
