@@ -68,6 +68,8 @@ extern "C" {
 #define ATTN_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed; see attn_strerror */
 #define ATTN_ERR_TIMEOUT (-5)     /* a kernel reported a bounded wait that expired */
 #define ATTN_ERR_DEVICE (-6)      /* a kernel reported an internal consistency error */
+#define ATTN_ERR_SCRATCH (-7)     /* attn_fwd_splitkv_noalloc: the problem needs more
+                                     scratch than its fixed array holds */
 
 /*
  * attn_fwd - fused attention forward, FP16 or BF16.
@@ -170,6 +172,40 @@ size_t attn_splitkv_workspace_bytes(int B, int Hq, int64_t Nq, int d, int num_sp
  * the current device for these sizes (at least 1, at most one per key tile,
  * at most 256).  Performs the one-time device set-up if needed. */
 int attn_splitkv_default_splits(int B, int Hq, int64_t Nq, int64_t Nk, int d);
+
+/*
+ * attn_fwd_splitkv_noalloc - attn_fwd_splitkv for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is an
+ * interface for a kind of caller, not part of the method.
+ *
+ * Who needs it: code that runs while a CUDA graph is being captured, programs
+ * whose device memory is owned by their own pool or arena, and services that
+ * forbid allocation on the request path.  attn_fwd_splitkv needs a workspace
+ * and the other entry points allocate a status word on their first call on a
+ * device; this one allocates nothing.  Its per-split partial results and its
+ * status word live in a fixed device array of 16 MiB that is part of the
+ * library (every GPU that loads the library holds it until the process
+ * exits).  The caller passes inputs and outputs exactly as for
+ * attn_fwd_splitkv, without a workspace.
+ *
+ * Limit: num_splits x B x Hq x Nq x (d + 1) x 4 bytes, the first part padded to
+ * 256 bytes, must fit in 16 MiB - 256 bytes (e.g. 256 splits of one query per
+ * head at Hq = 64, d = 128); otherwise ATTN_ERR_SCRATCH and nothing runs.
+ * With an effective split count of 1 (Nk <= 128 keys, or num_splits = 1) the
+ * scratch is not used.
+ * Set-up: the first call on a device reads device attributes, resolves the
+ * tensor-map encoder, looks up the array's device address
+ * (cudaGetSymbolAddress) and zeroes the status word with a synchronous
+ * cudaMemset; make that first call before any stream capture.
+ * Sharing: every call on a device uses the same array and it keeps the last
+ * call's contents; calls whose kernels overlap on the GPU (for example on two
+ * streams) race on it.  A bounded-wait timeout inside its kernels is recorded
+ * in the array's status word, which attn_get_status does not read.
+ * Errors as attn_fwd_splitkv, plus ATTN_ERR_SCRATCH.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d, int num_splits,
+                             float scale, int dtype, void* stream);
 
 /*
  * attn_get_status - synchronise `stream`, then read and clear the device

@@ -21,10 +21,11 @@ ATTN_F16, ATTN_BF16 = 0, 1
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED = -1, -2, -3
 ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = -4, -5, -6
+ERR_SCRATCH = -7
 
 EXPORTS = ("attn_fwd", "attn_prep_fp8", "attn_fwd_fp8", "attn_get_status", "attn_strerror",
            "attn_launch_count", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
-           "attn_splitkv_default_splits")
+           "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc")
 
 _lib = None
 
@@ -63,6 +64,9 @@ def load():
                                      i32, vp, ctypes.c_size_t, vp]
     lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_splitkv_workspace_bytes.argtypes = [i32, i32, i64, i32, i32]
+    lib.attn_fwd_splitkv_noalloc.restype = i32
+    lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32,
+                                             f32, i32, vp]
     lib.attn_splitkv_default_splits.restype = i32
     lib.attn_splitkv_default_splits.argtypes = [i32, i32, i64, i64, i32]
     _lib = lib

@@ -365,6 +365,7 @@ extern "C" const char* attn_strerror(int code) {
     case ATTN_ERR_CUDA: return g_cuda_msg;
     case ATTN_ERR_TIMEOUT: return "a kernel wait expired (bounded wait timeout)";
     case ATTN_ERR_DEVICE: return "a kernel reported an internal consistency error";
+    case ATTN_ERR_SCRATCH: return "problem needs more scratch than the fixed no-alloc array holds";
     default: return "unknown error code";
   }
 }
