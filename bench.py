@@ -312,7 +312,7 @@ def make_step(wl, dev):
     meta["d2h"] = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
     if kind == "decode":
-        splits = attn.splitkv_default_splits(B, Hq, Nq, Nk, d)
+        splits = attn.splitkv_default_splits(B, Hq, Hkv, Nq, Nk, d)
         ws = torch.empty(attn.splitkv_workspace_bytes(B, Hq, Nq, d, splits), dtype=torch.uint8,
                          device=dev)
 

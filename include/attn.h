@@ -148,7 +148,9 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q
  * CTAs; each leaves its O / l and LSE in FP32 in `workspace`, and a second
  * kernel combines them with the streaming-softmax merge rule of
  * "FlashAttention（V3）深度解析" section 4.2 (m = max(m_a, m_b),
- * z = z_a e^(m_a - m) + z_b e^(m_b - m)).  Same tensors, layouts and results
+ * z = z_a e^(m_a - m) + z_b e^(m_b - m)).  When Hq / Hkv divides 128, the
+ * query heads of a GQA group share the rows of one query tile, so each
+ * key/value head is read once per split.  Same tensors, layouts and results
  * as attn_fwd with causal = 0 (up to FP32 rounding of the merge).
  *   num_splits  >= 1; more splits than 128-key tiles are reduced to one per
  *               tile; an effective count of 1 runs attn_fwd's kernel alone
@@ -171,7 +173,7 @@ size_t attn_splitkv_workspace_bytes(int B, int Hq, int64_t Nq, int d, int num_sp
 /* attn_splitkv_default_splits - a split count that gives one wave of CTAs on
  * the current device for these sizes (at least 1, at most one per key tile,
  * at most 256).  Performs the one-time device set-up if needed. */
-int attn_splitkv_default_splits(int B, int Hq, int64_t Nq, int64_t Nk, int d);
+int attn_splitkv_default_splits(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d);
 
 /*
  * attn_fwd_splitkv_noalloc - attn_fwd_splitkv for callers that cannot

@@ -72,3 +72,14 @@ def test_splitkv_rejects_small_workspace(gpu_lib):
                               lse.data_ptr(), 1, 2, 2, 4, 4096, 128, 0, 0.1, 1, None, 0,
                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == -1   # num_splits < 1
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 1), (16, 1), (12, 4)])
+def test_splitkv_group_packing_and_fallback(gpu_lib, Hq, Hkv):
+    """Groups that divide 128 share query tiles (16/1); others (6/1, 12/4 with a
+    group of 3) run one head per tile.  Both must match the oracle."""
+    q, k, v = _inputs(2, 9, 3000, Hq, Hkv, 128, seed=16)
+    o, lse = gpu_lib.attn_fwd_splitkv(q, k, v, num_splits=5)
+    assert gpu_lib.get_status() == 0
+    o_ref, lse_ref = oracle_for(q, k, v, False, 1 / math.sqrt(128))
+    assert_within(errors(o, lse, o_ref, lse_ref))

@@ -68,7 +68,7 @@ def load():
     lib.attn_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i64, i32, i32,
                                              f32, i32, vp]
     lib.attn_splitkv_default_splits.restype = i32
-    lib.attn_splitkv_default_splits.argtypes = [i32, i32, i64, i64, i32]
+    lib.attn_splitkv_default_splits.argtypes = [i32, i32, i32, i64, i64, i32]
     _lib = lib
     return lib
 
@@ -139,8 +139,8 @@ def splitkv_workspace_bytes(B, Hq, Nq, d, num_splits) -> int:
     return int(load().attn_splitkv_workspace_bytes(B, Hq, Nq, d, num_splits))
 
 
-def splitkv_default_splits(B, Hq, Nq, Nk, d) -> int:
-    return int(load().attn_splitkv_default_splits(B, Hq, Nq, Nk, d))
+def splitkv_default_splits(B, Hq, Hkv, Nq, Nk, d) -> int:
+    return int(load().attn_splitkv_default_splits(B, Hq, Hkv, Nq, Nk, d))
 
 
 def attn_fwd_splitkv(q, k, v, num_splits: int | None = None, scale: float | None = None,
@@ -155,7 +155,7 @@ def attn_fwd_splitkv(q, k, v, num_splits: int | None = None, scale: float | None
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
     if num_splits is None:
-        num_splits = splitkv_default_splits(B, Hq, Nq, Nk, d)
+        num_splits = splitkv_default_splits(B, Hq, Hkv, Nq, Nk, d)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:

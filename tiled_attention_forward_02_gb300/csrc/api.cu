@@ -85,14 +85,15 @@ int encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const cuu
   return ATTN_OK;
 }
 
-// BSHD tensor [B, N, H, d] as TMA dims (d, H, N, B); box = one head, 128 rows,
-// `inner` elements of d (128 bytes for the 128-byte swizzle)
+// BSHD tensor [B, N, H, d] as TMA dims (d, H, N, B); box = `heads` heads x
+// 128 / heads rows (128 rows of 128 bytes in all), `inner` elements of d
+// (128 bytes for the 128-byte swizzle)
 int map_bshd(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* base, int B, int64_t N,
-             int H, int d, int inner) {
+             int H, int d, int inner, int heads = 1) {
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)d * esz, (cuuint64_t)H * d * esz,
                                  (cuuint64_t)N * H * d * esz};
-  const cuuint32_t box[4] = {(cuuint32_t)inner, 1, 128, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)heads, (cuuint32_t)(128 / heads), 1};
   return encode(map, dt, base, dims, strides, box);
 }
 
@@ -119,10 +120,12 @@ int check_common(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int causal, flo
 }
 
 int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, float scale,
-                const DeviceState& st, int* grid, int n_splits = 1, int split_tiles = 0) {
+                const DeviceState& st, int* grid, int n_splits = 1, int split_tiles = 0,
+                int pack_g = 1) {
   const int qst = fwd_q_tiles(d);
-  const int64_t n_mb = (Nq + qst * 128 - 1) / (qst * 128);
-  const int64_t units = (int64_t)B * Hq * n_mb * n_splits;
+  // pack_g query heads share each tile: Nq * pack_g packed rows per head group
+  const int64_t n_mb = (Nq * pack_g + qst * 128 - 1) / (qst * 128);
+  const int64_t units = (int64_t)B * (Hq / pack_g) * n_mb * n_splits;
   if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   p.B = B;
   p.Hq = Hq;
@@ -137,7 +140,8 @@ int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t
   p.nkb = (int)((Nk + 127) / 128);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st.status;
-  p.active_stages = (Nq <= 128) ? 1 : qst;   // the second query tile would hold only padding
+  p.active_stages = (Nq * pack_g <= 128) ? 1 : qst;   // a second tile would hold only padding
+  p.pack_g = pack_g;
   p.n_splits = n_splits;
   p.split_tiles = split_tiles > 0 ? split_tiles : p.n_kv_tiles;
   *grid = (int)(units < st.sm_count ? units : st.sm_count);
@@ -273,12 +277,16 @@ extern "C" size_t attn_splitkv_workspace_bytes(int B, int Hq, int64_t Nq, int d,
   return (size_t)splitkv_bytes(B, Hq, Nq, d, num_splits);
 }
 
-extern "C" int attn_splitkv_default_splits(int B, int Hq, int64_t Nq, int64_t Nk, int d) {
-  if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1) return 1;
+extern "C" int attn_splitkv_default_splits(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk,
+                                           int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 1 || Nk < 1) return 1;
   DeviceState* st = nullptr;
   if (device_state(&st) != ATTN_OK) return 1;
   const int qst = fwd_q_tiles(d);
-  const int64_t units = (int64_t)B * Hq * ((Nq + qst * 128 - 1) / (qst * 128));
+  const int group = Hq / Hkv;
+  const int pack_g = (group <= 128 && 128 % group == 0) ? group : 1;   // as attn_fwd_splitkv
+  const int64_t units =
+      (int64_t)B * (Hq / pack_g) * ((Nq * pack_g + qst * 128 - 1) / (qst * 128));
   const int64_t tiles = (Nk + 127) / 128;
   int64_t n = (st->sm_count + units - 1) / units;   // enough units for one wave
   if (n > tiles) n = tiles;
@@ -309,10 +317,14 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
   }
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  // the split instance packs a GQA group into the rows of one query tile so
+  // that each key/value head is streamed once per split
+  const int group = Hq / Hkv;
+  const int pack_g = (eff > 1 && group <= 128 && 128 % group == 0) ? group : 1;
   const CUtensorMapDataType tdt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
-  if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64)) ||
+  if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64, pack_g)) ||
       (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64)) ||
       (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64)))
     return rc;
@@ -320,7 +332,8 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
   p.o = o;
   p.lse = lse;
   int grid = 0;
-  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid, eff, split_tiles)) != ATTN_OK)
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid, eff, split_tiles, pack_g)) !=
+      ATTN_OK)
     return rc;
   float* o_part = nullptr;
   float* lse_part = nullptr;

@@ -73,6 +73,9 @@ struct FwdParams {
   int n_splits;            // 1: no split, results go to o / lse
   int split_tiles;         // key tiles per split
   float* o_part;           // [n_splits, B, Hq, Nq, D] O / l of the split (n_splits > 1)
+  // split instances: query heads packed into the rows of one tile (a GQA
+  // group, or 1); tile row r is position m0 + r / pack_g of head hq + r % pack_g
+  int pack_g;
   float* lse_part;         // [n_splits, B, Hq, Nq] natural-log LSE of the split
 };
 
@@ -143,7 +146,7 @@ __host__ __device__ constexpr uint32_t idesc_make(uint32_t fmt, int M, int N, bo
 
 // ----------------------------------------------------------------- scheduling
 struct Unit {
-  int b, hq, hk, m0;
+  int b, hq, hk, m0;   // hq: first query head of the unit; m0: first query position
   int j0;       // first key tile of the unit's key range
   int sp;       // split index
   int n_s[2];   // key tiles each query tile visits
@@ -169,10 +172,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& p) {
     bh = v / p.n_mblocks;
     mb = v % p.n_mblocks;
   }
-  U.b = bh / p.Hq;
-  U.hq = bh % p.Hq;
+  const int G = SPLIT ? p.pack_g : 1;   // query heads per tile row group
+  const int HP = p.Hq / G;                // packed head groups
+  U.b = bh / HP;
+  U.hq = (bh % HP) * G;
   U.hk = U.hq / p.group;
-  U.m0 = mb * QST * 128;
+  U.m0 = mb * QST * (128 / G);
   U.j0 = SPLIT ? U.sp * p.split_tiles : 0;
   U.n = 0;
 #pragma unroll
@@ -274,6 +279,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   // query tiles that hold rows: only the split (decode) instances skip an
   // all-padding second tile; the others keep the count a compile-time constant
   const int n_active = SPLIT ? (QST < p.active_stages ? QST : p.active_stages) : QST;
+  const int G = SPLIT ? p.pack_g : 1;   // query heads packed per tile row group
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
           ptx::mbar_arrive_expect_tx(bar(B_QFULL + s), C::QBYTES);
           for (int ch = 0; ch < C::NCH; ++ch)
             ptx::tma_load_4d(sQ + s * C::QBYTES + ch * C::CHUNK_BYTES, &tmQ, bar(B_QFULL + s),
-                             ch * C::CH_ELEMS, U.hq, U.m0 + s * 128, U.b);
+                             ch * C::CH_ELEMS, U.hq, U.m0 + s * (128 / G), U.b);
         }
         for (int j = 0; j < U.n && ok; ++j) {
           // K_j
@@ -479,8 +485,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       if (u == -2) break;
       if (u < 0) continue;
       const Unit U = decode_unit<QST, CAUSAL, SPLIT>(u, p);
-      const int m_s = U.m0 + s * 128;
-      const int row = m_s + r;
+      const int m_s = U.m0 + s * (128 / G);   // first query position of this tile
+      const int row = m_s + r / G;            // query position of this thread's row
+      const int hrow = U.hq + r % G;          // query head of this thread's row
       const int ns = U.n_s[s];
 
       float qd = 1.f, vref = 1.f;
@@ -646,7 +653,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       const float lse_row = (mi + ptx::lg2(li) - C::PSHIFT) * 0.6931471805599453f;
       if constexpr (SPLIT) {
         // partial result of this key range: FP32 O / l and its LSE
-        const long long prow = (((long long)U.sp * p.B + U.b) * p.Hq + U.hq) * p.Nq + row;
+        const long long prow = (((long long)U.sp * p.B + U.b) * p.Hq + hrow) * p.Nq + row;
         float* dst = p.o_part + prow * D;
 #pragma unroll 1
         for (int cb = 0; cb < D; cb += 32) {
@@ -664,7 +671,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         if (live) p.lse_part[prow] = lse_row;
       } else {
         uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                         (((long long)U.b * p.Nq + row) * p.Hq + U.hq) * D;
+                         (((long long)U.b * p.Nq + row) * p.Hq + hrow) * D;
 #pragma unroll 1
         for (int cb = 0; cb < D; cb += 32) {
           uint32_t o32[32];
@@ -683,7 +690,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
               dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           }
         }
-        if (live) p.lse[((long long)U.b * p.Hq + U.hq) * p.Nq + row] = lse_row;
+        if (live) p.lse[((long long)U.b * p.Hq + hrow) * p.Nq + row] = lse_row;
       }
       ptx::tc_fence_before();
       __syncwarp();

@@ -80,11 +80,11 @@ int noalloc_setup(NoAllocDevice** out) {
 }
 
 int na_map_bshd(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int B, int64_t N,
-                int H, int d) {
+                int H, int d, int heads = 1) {
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2,
                                  (cuuint64_t)N * H * d * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)heads, (cuuint32_t)(128 / heads), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_na_encode(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -129,14 +129,16 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   int rc = noalloc_setup(&st);
   if (rc != ATTN_OK) return rc;
   const int qst = fwd_q_tiles(d);
-  const int64_t n_mb = (Nq + qst * 128 - 1) / (qst * 128);
-  const int64_t units = (int64_t)B * Hq * n_mb * eff;
+  const int group = Hq / Hkv;
+  const int pack_g = (eff > 1 && group <= 128 && 128 % group == 0) ? group : 1;
+  const int64_t n_mb = (Nq * pack_g + qst * 128 - 1) / (qst * 128);
+  const int64_t units = (int64_t)B * (Hq / pack_g) * n_mb * eff;
   if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
 
   const CUtensorMapDataType tdt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
-  if ((rc = na_map_bshd(&mq, tdt, q, B, Nq, Hq, d)) ||
+  if ((rc = na_map_bshd(&mq, tdt, q, B, Nq, Hq, d, pack_g)) ||
       (rc = na_map_bshd(&mk, tdt, k, B, Nk, Hkv, d)) ||
       (rc = na_map_bshd(&mv, tdt, v, B, Nk, Hkv, d)))
     return rc;
@@ -157,7 +159,8 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   p.nkb = tiles;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = reinterpret_cast<unsigned int*>(st->scratch);
-  p.active_stages = (Nq <= 128) ? 1 : qst;
+  p.active_stages = (Nq * pack_g <= 128) ? 1 : qst;
+  p.pack_g = pack_g;
   p.n_splits = eff;
   p.split_tiles = split_tiles;
   float* o_part = reinterpret_cast<float*>(st->scratch + kNoAllocStatusBytes);
