@@ -367,10 +367,18 @@ def make_step(wl, dev):
     kd = torch.empty((B, Hkv, (Nk + 127) // 128), dtype=torch.float32, device=dev)
     vd = torch.empty_like(kd)
 
+    prep_ev = []   # (start, end) events around the three prep calls of each timed step
+
     def step(kernel_events=None):
+        if kernel_events:
+            pe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            pe[0].record()
         attn.attn_prep_fp8(q, signs, Hkv if had else None, False, out=q8, descale=qd)
         attn.attn_prep_fp8(k, signs, Hkv if had else None, False, out=k8, descale=kd)
         attn.attn_prep_fp8(v, None, None, True, out=v8, descale=vd)
+        if kernel_events:
+            pe[1].record()
+            prep_ev.append(pe)
         if kernel_events:
             kernel_events[0].record()
         attn.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=causal, scale=scale, hadamard=had,
@@ -387,6 +395,9 @@ def make_step(wl, dev):
         hl.copy_(lse, non_blocking=True)
     meta["launches_per_step"] = 4
     meta["kernel"] = "attn_fwd_kernel<e4m3>"
+    meta["prep_events"] = prep_ev
+    # prep: every bf16 element read once, one E4M3 byte written, one descale per block
+    meta["prep_bytes"] = sum(t.numel() * 3 for t in (q, k, v)) + 4 * (qd.numel() + 2 * kd.numel())
     return step, e2e, meta
 
 
@@ -474,6 +485,14 @@ def gpu_arm(args, rank, world, local):
     cpu_tf, cpu_rows, cpu_s, cpu_threads = (None, 0, 0.0, 0)
     if not args.no_cpu_baseline:
         cpu_tf, cpu_rows, cpu_s, cpu_threads = time_oracle(wl, budget_s=args.cpu_budget)
+    prep = None
+    if meta.get("prep_events"):
+        pms = [a.elapsed_time(b) for a, b in meta["prep_events"]]
+        pms = sum(pms) / len(pms)
+        gbs = meta["prep_bytes"] / (pms * 1e-3) / 1e9
+        prep = {"kernel": "prep_fp8_kernel (Q, K, V)", "ms_per_step": pms, "bound": "hbm",
+                "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": meta["prep_bytes"]}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -491,6 +510,7 @@ def gpu_arm(args, rank, world, local):
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                 "h2d_bytes_per_step": meta["h2d"], "d2h_bytes_per_step": meta["d2h"]},
         "gpu_launches": launches,
+        "prep_roofline": prep,
         "kernel_ms": {"avg": avg_launch_ms, "min": min(per_launch_ms), "max": max(per_launch_ms)},
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "status": status,

@@ -106,7 +106,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *                                  transpose, section 7.4).
  *   descale  [B, H, ceil(N/128)] float32 (written): one scale per block of
  *            128 tokens x d of one (b, head); descale = amax / 448, or 1 for
- *            an all-zero block.  code = E4M3_RNE_satfinite(y / descale).
+ *            an all-zero block.  code = E4M3_RNE_satfinite(y * r) with
+ *            r = 448 / amax rounded to float32 once per block (1 for an
+ *            all-zero block) and the product rounded to float32.
  *   signs    NULL (no transform) or [sign_heads, d] int8 of +1/-1 (device).
  *            With signs, every row is replaced, before quantisation, by
  *            y = (x * sigma) H_d / sqrt(d) in float32, H_d the Sylvester

@@ -10,8 +10,10 @@ Sources and readings
   attention pipeline.  Reading taken: symmetric per-block scale, no offset
   (FP8 is sign-magnitude), one block = 128 tokens x d of one (batch, head);
   descale = amax / 448 (448 = largest finite E4M3 value), descale = 1 for an
-  all-zero block; code = E4M3(x / descale) rounded to nearest-even with
-  saturation to +-448.  The last block of a sequence may be partial.
+  all-zero block; code = E4M3(x * (448 / amax)) rounded to nearest-even with
+  saturation to +-448 (the reciprocal 448 / amax is rounded to float32 once
+  per block, as is the product).  The last block of a sequence may be
+  partial.
 * FP8 format: the pages say "FP8" (H100 FP8 tensor cores, 1978 TFLOPS, in
   the Together AI summary card "FlashAttention-3——利用异步与低精度加速注意力机制");
   the code on the dtcms.com page (section 11, FP8Support.fp32_to_fp8_conversion)
@@ -29,10 +31,10 @@ Sources and readings
   query heads of that group.
 
 Precision of the quantisation decision: the block amax, the descale
-amax / 448 and the quotient x / descale are taken in float32 with IEEE
-round-to-nearest, as the kernel does, so that codes can be compared bit for
-bit where the transformed values are themselves exact in float32 (no
-Hadamard).  With the Hadamard transform the oracle forms the product in
+amax / 448, the reciprocal 448 / amax and the product x * (448 / amax) are
+taken in float32 with IEEE round-to-nearest, as the kernel does, so that codes
+can be compared bit for bit where the transformed values are themselves exact
+in float32 (no Hadamard).  With the Hadamard transform the oracle forms the product in
 float64 and rounds once to float32.
 """
 from __future__ import annotations
@@ -131,8 +133,10 @@ def quantize_blocks(y32: np.ndarray, block: int = BLOCK):
         blk = y32[:, n0:n1]                                   # [B, n, H, d]
         amax = np.abs(blk).max(axis=(1, 3)).astype(np.float32)  # [B, H], exact
         ds = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        inv = np.where(amax > 0, np.float32(E4M3_MAX) / np.where(amax > 0, amax, np.float32(1.0)),
+                       np.float32(1.0)).astype(np.float32)
         descale[:, :, t] = ds
-        q = (blk / ds[:, None, :, None]).astype(np.float32)   # IEEE float32 quotient
+        q = (blk * inv[:, None, :, None]).astype(np.float32)  # IEEE float32 product
         codes[:, n0:n1] = e4m3_encode(q)
     return codes, descale
 

@@ -117,7 +117,12 @@ def test_fp8_forward_vs_dequantised_oracle(gpu_lib, causal, hadamard, d):
     e = errors(o, lse, o_ref, lse_ref)
     assert e["nonfinite"] == 0, e
     assert e["o_rel_rms"] <= 4e-2, e
-    assert e["lse_max_abs"] <= 2e-3, e
+    # without the transform both sides quantise identical float32 values (codes
+    # bit-exact); with it, the kernel's float32 butterfly and the oracle's
+    # float64 product may put a value on either side of an E4M3 rounding
+    # boundary (one code step, see test_prep_with_transform_matches_oracle),
+    # and on a x50-outlier row one such step moves the logits measurably
+    assert e["lse_max_abs"] <= (1e-2 if hadamard else 2e-3), e
 
 
 @pytest.mark.parametrize("outlier_scale", [50.0, 10.0])

@@ -98,7 +98,9 @@ def test_block_quantisation_properties():
                 dec = fp8.e4m3_decode(codes[b, t * 128:(t + 1) * 128, h])
                 # spacing of E4M3 at |q|: 2^(floor(log2|q|) - 3), at least 2^-9
                 e = np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6)))
-                assert np.all(np.abs(dec - q) <= 0.5 * np.exp2(e - 3) * (1 + 1e-6))
+                # (the scaled value is x * fl(448 / amax), within 2^-23 relative of
+                # x / descale, so a value on a rounding midpoint may round either way)
+                assert np.all(np.abs(dec - q) <= 0.5 * np.exp2(e - 3) * (1 + 1e-5))
                 assert np.abs(dec).max() == 448.0
 
 

@@ -243,7 +243,7 @@ extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int
   if (signs && (sign_heads < 1 || H % sign_heads != 0)) return ATTN_ERR_INVALID_ARG;
   if (N > kMaxRows) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
-  if (B > 65535 || H > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y/z limits
+  if (B > 65535 || (N + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;  // grid y/z limits
   if (B == 0 || N == 0) return ATTN_OK;
   if (!x || !x8 || !descale) return ATTN_ERR_INVALID_ARG;
   if (!aligned(x, 128) || !aligned(x8, 128) || !aligned(descale, 16)) return ATTN_ERR_MISALIGNED;

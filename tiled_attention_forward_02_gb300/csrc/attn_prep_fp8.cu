@@ -7,11 +7,14 @@
 // incoherent processing (each head multiplied by a random orthogonal matrix,
 // Hadamard x random signs, to spread outliers before quantisation).
 //
-// One CTA per (128-token block, head, batch); 8 warps x 16 rows; a warp holds
-// one row of d values (d/32 per lane).  The transform is a fast Walsh-Hadamard
-// butterfly (in-lane stages, then lane shuffles), scaled by 1/sqrt(d); the
-// block amax is reduced through shared memory; codes are y / descale rounded
-// to nearest-even and saturated to +-448 by the hardware conversion.  The
+// One CTA per (128-token block, head, batch); 8 warps x 16 rows; a half warp
+// holds one row (d/16 values per lane, loaded 16 bytes at a time, all rows of
+// the block in flight before any arithmetic).  The transform is a fast
+// Walsh-Hadamard butterfly (in-lane stages, then shuffles within the half
+// warp), scaled by 1/sqrt(d); the
+// block amax is reduced through shared memory; codes are y * (448 / amax)
+// (float32, the reciprocal rounded once per block) rounded to nearest-even and
+// saturated to +-448 by the hardware conversion; descale = amax / 448.  The
 // kernel is bandwidth-bound: it reads each bf16 element once and writes one
 // byte per element.
 #include <cuda_bf16.h>
@@ -23,6 +26,28 @@
 
 namespace attn {
 
+// 16 bytes of bf16 input per lane; a half warp holds one row
+template <int D>
+__device__ __forceinline__ void load_row_part(const uint16_t* src, float (&y)[D / 16]) {
+  constexpr int VEC = D / 16;
+  if constexpr (VEC == 4) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
+    y[0] = __uint_as_float(w.x << 16); y[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    y[2] = __uint_as_float(w.y << 16); y[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  } else {
+#pragma unroll
+    for (int q = 0; q < VEC / 8; ++q) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + q);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        y[8 * q + 2 * i] = __uint_as_float(ws[i] << 16);
+        y[8 * q + 2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restrict__ x,
                                                        uint8_t* __restrict__ x8,
@@ -30,83 +55,71 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restric
                                                        const int8_t* __restrict__ signs,
                                                        int sign_group, int H, int N, int nb,
                                                        int Npad, int transpose_out) {
-  constexpr int VEC = D / 32;  // elements per lane
-  constexpr int ROWS = 16;     // rows per warp
+  constexpr int VEC = D / 16;  // elements per lane (a half warp covers one row)
+  constexpr int ITERS = 8;     // 8 warps x 2 rows x 8 iterations = 128 rows
   __shared__ float s_amax[8];
   __shared__ __align__(16) uint8_t s_t[D * 128];  // transposed block (channel-major)
 
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // heads vary fastest across the grid, so that CTAs running together read
+  // neighbouring pieces of the same token rows ([B, N, H, d] layout)
+  const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e0 = lane * VEC;  // first channel of this lane
+  const int half = lane >> 4, hl = lane & 15;
+  const int e0 = hl * VEC;  // first channel of this lane
+  // row of iteration i: blk*128 + warp*16 + 2i + half
+  auto row_of = [&](int i) { return blk * 128 + warp * 16 + 2 * i + half; };
 
   float sg[VEC];
 #pragma unroll
   for (int v = 0; v < VEC; ++v)
     sg[v] = signs ? (float)signs[(long long)(h / sign_group) * D + e0 + v] : 1.f;
 
-  float y[ROWS][VEC];
-  float amax = 0.f;
+  float y[ITERS][VEC];
+  // issue every load of the block before any arithmetic on it
 #pragma unroll
-  for (int rr = 0; rr < ROWS; ++rr) {
-    const int n = blk * 128 + warp * ROWS + rr;
-    uint16_t raw[VEC];
+  for (int i = 0; i < ITERS; ++i) {
+    const int n = row_of(i);
     if (n < N) {
-      const uint16_t* src = x + (((long long)b * N + n) * H + h) * D + e0;
-      if constexpr (VEC == 2) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
-        raw[0] = (uint16_t)(w & 0xFFFF);
-        raw[1] = (uint16_t)(w >> 16);
-      } else if constexpr (VEC == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(src);
-        raw[0] = (uint16_t)(w.x & 0xFFFF); raw[1] = (uint16_t)(w.x >> 16);
-        raw[2] = (uint16_t)(w.y & 0xFFFF); raw[3] = (uint16_t)(w.y >> 16);
-      } else {
-        const uint4 w = *reinterpret_cast<const uint4*>(src);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          raw[2 * q] = (uint16_t)(ws[q] & 0xFFFF);
-          raw[2 * q + 1] = (uint16_t)(ws[q] >> 16);
-        }
-      }
+      load_row_part<D>(x + (((long long)b * N + n) * H + h) * D + e0, y[i]);
     } else {
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) raw[v] = 0;
+      for (int v = 0; v < VEC; ++v) y[i][v] = 0.f;
     }
+  }
+  float amax = 0.f;
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) y[rr][v] = __uint_as_float((uint32_t)raw[v] << 16);
-
+  for (int i = 0; i < ITERS; ++i) {
     if (signs) {
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) y[rr][v] *= sg[v];
+      for (int v = 0; v < VEC; ++v) y[i][v] *= sg[v];
       // butterfly stages inside the lane (channel bit < log2 VEC)
 #pragma unroll
       for (int hs = 1; hs < VEC; hs <<= 1) {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
           if ((v & hs) == 0) {
-            const float a = y[rr][v], c = y[rr][v + hs];
-            y[rr][v] = a + c;
-            y[rr][v + hs] = a - c;
+            const float a = y[i][v], c = y[i][v + hs];
+            y[i][v] = a + c;
+            y[i][v + hs] = a - c;
           }
         }
       }
-      // butterfly stages across lanes (channel bit >= log2 VEC)
+      // butterfly stages across the 16 lanes of the half warp
 #pragma unroll
-      for (int lm = 1; lm < 32; lm <<= 1) {
-        const bool upper = (lane & lm) != 0;
+      for (int lm = 1; lm < 16; lm <<= 1) {
+        const bool upper = (hl & lm) != 0;
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-          const float other = __shfl_xor_sync(0xffffffffu, y[rr][v], lm);
-          y[rr][v] = upper ? (other - y[rr][v]) : (y[rr][v] + other);
+          const float other = __shfl_xor_sync(0xffffffffu, y[i][v], lm);
+          y[i][v] = upper ? (other - y[i][v]) : (y[i][v] + other);
         }
       }
       const float inv_sqrt_d = (D == 64) ? 0.125f : (D == 128) ? 0.08838834764831845f : 0.0625f;
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) y[rr][v] *= inv_sqrt_d;
+      for (int v = 0; v < VEC; ++v) y[i][v] *= inv_sqrt_d;
     }
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) amax = fmaxf(amax, fabsf(y[rr][v]));
+    for (int v = 0; v < VEC; ++v) amax = fmaxf(amax, fabsf(y[i][v]));
   }
 
 #pragma unroll
@@ -117,37 +130,37 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restric
 #pragma unroll
   for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, s_amax[w]);
   const float ds = bmax > 0.f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
+  // codes are y * (448 / amax), the reciprocal taken once per block
+  const float inv_ds = bmax > 0.f ? __fdiv_rn(448.0f, bmax) : 1.0f;
   if (threadIdx.x == 0) descale[((long long)b * H + h) * nb + blk] = ds;
 
 #pragma unroll
-  for (int rr = 0; rr < ROWS; ++rr) {
-    const int nl = warp * ROWS + rr;
-    const int n = blk * 128 + nl;
-    float qv[VEC];
+  for (int i = 0; i < ITERS; ++i) {
+    const int n = row_of(i);
+    const int nl = n - blk * 128;
+    uint32_t c4[VEC / 4];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) qv[v] = __fdiv_rn(y[rr][v], ds);
+    for (int q = 0; q < VEC / 4; ++q)
+      c4[q] = ptx::pack_e4m3x4(y[i][4 * q] * inv_ds, y[i][4 * q + 1] * inv_ds,
+                               y[i][4 * q + 2] * inv_ds, y[i][4 * q + 3] * inv_ds);
     if (!transpose_out) {
       if (n < N) {
         uint8_t* dst = x8 + (((long long)b * N + n) * H + h) * D + e0;
-        if constexpr (VEC == 2) {
-          const uint32_t c4 = ptx::pack_e4m3x4(qv[0], qv[1], 0.f, 0.f);
-          *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(c4 & 0xFFFF);
-        } else if constexpr (VEC == 4) {
-          *reinterpret_cast<uint32_t*>(dst) = ptx::pack_e4m3x4(qv[0], qv[1], qv[2], qv[3]);
+        if constexpr (VEC == 4) {
+          *reinterpret_cast<uint32_t*>(dst) = c4[0];
+        } else if constexpr (VEC == 8) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(c4[0], c4[1]);
         } else {
-          uint2 w;
-          w.x = ptx::pack_e4m3x4(qv[0], qv[1], qv[2], qv[3]);
-          w.y = ptx::pack_e4m3x4(qv[4], qv[5], qv[6], qv[7]);
-          *reinterpret_cast<uint2*>(dst) = w;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
         }
       }
     } else {
-      // stage codes channel-major: s_t[e][nl]; rows n >= N hold zeros
+      // stage codes channel-major: s_t[e][nl ^ swz(e)] (rows n >= N hold zeros);
+      // the XOR swizzle puts the 16 channels a half warp writes in distinct banks
 #pragma unroll
-      for (int v = 0; v < VEC; v += 2) {
-        const uint32_t c4 = ptx::pack_e4m3x4(qv[v], qv[v + 1], 0.f, 0.f);
-        s_t[(e0 + v) * 128 + nl] = (uint8_t)(c4 & 0xFF);
-        s_t[(e0 + v + 1) * 128 + nl] = (uint8_t)((c4 >> 8) & 0xFF);
+      for (int v = 0; v < VEC; ++v) {
+        const int e = e0 + v;
+        s_t[e * 128 + (nl ^ (((e / VEC) & 31) << 2))] = (uint8_t)((c4[v >> 2] >> (8 * (v & 3))) & 0xFF);
       }
     }
   }
@@ -159,7 +172,7 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restric
       if (lane * 4 < valid) {
         uint8_t* dst = x8 + (((long long)b * H + h) * D + e) * Npad + blk * 128 + lane * 4;
         *reinterpret_cast<uint32_t*>(dst) =
-            *reinterpret_cast<const uint32_t*>(&s_t[e * 128 + lane * 4]);
+            *reinterpret_cast<const uint32_t*>(&s_t[e * 128 + ((lane * 4) ^ (((e / VEC) & 31) << 2))]);
       }
     }
   }
@@ -169,7 +182,7 @@ int launch_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int N
                     const int8_t* signs, int sign_group, int transpose_out, cudaStream_t stream) {
   const int nb = (N + 127) / 128;
   const int Npad = (N + 15) / 16 * 16;
-  dim3 grid(nb, H, B);
+  dim3 grid(H, nb, B);
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint8_t* xo = static_cast<uint8_t*>(x8);
   switch (d) {
