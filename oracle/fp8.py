@@ -30,6 +30,23 @@ Sources and readings
   sigma_h in {+1, -1}^d is an input, one row per key/value head, shared by the
   query heads of that group.
 
+* Per-tensor FP8 (the baseline of the error comparison): the summary card,
+  same section, says incoherent processing gives 2.6 times lower error than
+  "baseline FP8" without naming that baseline.  Reading taken: one scale for
+  the whole tensor (all batches, heads and tokens), descale = amax / 448,
+  codes and the float32 reciprocal and product as for a block.  The descale
+  is written for every (b, head, block) so that the same forward consumes
+  either scheme.
+* Rotary embedding fused with the transform: the summary card, same section,
+  says the Hadamard transform can be fused with rotary embedding (a
+  bandwidth-bound step) at no extra cost.  The pages define no rotary
+  variant.  Reading taken: the rotate-half form, channel c paired with
+  c + d/2 for c < d/2, angle (pos0 + n) * base^(-2c/d) for token n, base
+  10000 by default; (x_c, x_{c+d/2}) -> (x_c cos - x_{c+d/2} sin,
+  x_{c+d/2} cos + x_c sin).  It is applied to Q and K before the Hadamard
+  transform (the rotation must act on the model's own Q and K; M is applied
+  after it so that Q M (K M)^T is still the rotated Q K^T), never to V.
+
 Precision of the quantisation decision: the block amax, the descale
 amax / 448, the reciprocal 448 / amax and the product x * (448 / amax) are
 taken in float32 with IEEE round-to-nearest, as the kernel does, so that codes
@@ -141,19 +158,67 @@ def quantize_blocks(y32: np.ndarray, block: int = BLOCK):
     return codes, descale
 
 
-def prepare(x, signs=None, hadamard: bool = False):
+def quantize_tensor(y32: np.ndarray, block: int = BLOCK):
+    """One symmetric scale for the whole tensor (the per-tensor FP8 baseline).
+
+    y32 : [B, N, H, d] float32.  Returns (codes uint8 [B, N, H, d], descale
+    float32 [B, H, ceil(N/block)]) with every descale equal to amax / 448 (1
+    for an all-zero tensor), amax taken over every element."""
+    y32 = np.asarray(y32, dtype=np.float32)
+    B, N, H, d = y32.shape
+    nb = (N + block - 1) // block
+    amax = np.float32(np.abs(y32).max()) if y32.size else np.float32(0.0)
+    if amax > 0:
+        ds = np.float32(amax / np.float32(E4M3_MAX))
+        inv = np.float32(np.float32(E4M3_MAX) / amax)
+    else:
+        ds = inv = np.float32(1.0)
+    codes = e4m3_encode((y32 * inv).astype(np.float32))   # IEEE float32 product
+    return codes, np.full((B, H, nb), ds, dtype=np.float32)
+
+
+def rope_tables(N: int, d: int, base: float = 10000.0, pos0: int = 0):
+    """cos and sin of the rotary angles, float64 [N, d/2]:
+    angle[n, c] = (pos0 + n) * base^(-2c/d)."""
+    if d % 2:
+        raise ValueError("d must be even")
+    c = np.arange(d // 2, dtype=np.float64)
+    freq = np.power(np.float64(base), -2.0 * c / d)
+    ang = (pos0 + np.arange(N, dtype=np.float64))[:, None] * freq[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def rope(x, base: float = 10000.0, pos0: int = 0) -> np.ndarray:
+    """Rotate-half rotary embedding of x [B, N, H, d] in float64: channel c
+    and c + d/2 rotate by angle[n, c] (see rope_tables)."""
+    x = np.asarray(x, dtype=np.float64)
+    B, N, H, d = x.shape
+    cos, sin = rope_tables(N, d, base, pos0)
+    cos, sin = cos[None, :, None, :], sin[None, :, None, :]
+    a, b = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([a * cos - b * sin, b * cos + a * sin], axis=-1)
+
+
+def prepare(x, signs=None, hadamard: bool = False, per_tensor: bool = False,
+            rope_base: float | None = None, rope_pos0: int = 0):
     """The oracle of the FP8 preparation step on one tensor [B, N, H, d].
 
-    x is the exact input (bf16 values as float32/float64).  Returns
-    (codes uint8 [B, N, H, d], descale float32 [B, H, nblocks], y32) where y32
-    is the float32 tensor that was quantised."""
+    x is the exact input (bf16 values as float32/float64).  Steps, in order:
+    rotary embedding (when rope_base is given), the Hadamard transform (when
+    hadamard), rounding to float32, then per-block (default) or per-tensor
+    quantisation.  Returns (codes uint8 [B, N, H, d], descale float32
+    [B, H, nblocks], y32) where y32 is the float32 tensor that was quantised."""
     x = np.asarray(x)
-    if hadamard:
-        y = incoherent_transform(x, signs)
-        y32 = y.astype(np.float32)
-    else:
+    if rope_base is None and not hadamard:
         y32 = np.asarray(x, dtype=np.float32)
-    codes, ds = quantize_blocks(y32)
+    else:
+        y = np.asarray(x, dtype=np.float64)
+        if rope_base is not None:
+            y = rope(y, rope_base, rope_pos0)
+        if hadamard:
+            y = incoherent_transform(y, signs)
+        y32 = y.astype(np.float32)
+    codes, ds = quantize_tensor(y32) if per_tensor else quantize_blocks(y32)
     return codes, ds, y32
 
 

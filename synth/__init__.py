@@ -11,6 +11,11 @@ Recipe (every workload):
 * Outlier injection (the FP8 workload): after each tensor's normal draw, a
   uniform draw from the same generator selects entries with probability
   ``outlier_frac`` (0.1 %), which are multiplied by ``outlier_scale`` (50).
+* Channel outliers (a second outlier structure for the FP8 error study):
+  from a CPU generator seeded with ``seed + 11``, ``channel_outliers``
+  channels are chosen per key/value head (a random permutation's first
+  entries); every token's value in them is multiplied by ``channel_scale`` in
+  K and in the query heads of that group; V is left as drawn.
 * Hadamard signs: +-1 per (key/value head, channel) from a generator seeded
   with ``seed + 7``.
 * Sampled query rows: uniform per (b, h) from a generator seeded with
@@ -30,8 +35,15 @@ def _draw(shape, gen, device, outlier_frac, outlier_scale):
     return t
 
 
+def _channel_mult(Hkv, d, gen, n_channels, scale):
+    mult = torch.ones(Hkv, d, dtype=torch.float32)
+    for h in range(Hkv):
+        mult[h, torch.randperm(d, generator=gen)[:n_channels]] = scale
+    return mult
+
+
 def attn_inputs(B, Nq, Nk, Hq, Hkv, d, dtype=torch.bfloat16, seed=0, device="cpu",
-                outlier_frac=0.0, outlier_scale=50.0):
+                outlier_frac=0.0, outlier_scale=50.0, channel_outliers=0, channel_scale=10.0):
     """Return (q, k, v) in BSHD with the given dtype on ``device``.
 
     With ``device='cuda'`` the draw uses a CUDA generator (a different but
@@ -39,10 +51,15 @@ def attn_inputs(B, Nq, Nk, Hq, Hkv, d, dtype=torch.bfloat16, seed=0, device="cpu
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
     gen.manual_seed(int(seed))
-    q = _draw((B, Nq, Hq, d), gen, dev, outlier_frac, outlier_scale).to(dtype)
-    k = _draw((B, Nk, Hkv, d), gen, dev, outlier_frac, outlier_scale).to(dtype)
-    v = _draw((B, Nk, Hkv, d), gen, dev, outlier_frac, outlier_scale).to(dtype)
-    return q, k, v
+    q = _draw((B, Nq, Hq, d), gen, dev, outlier_frac, outlier_scale)
+    k = _draw((B, Nk, Hkv, d), gen, dev, outlier_frac, outlier_scale)
+    v = _draw((B, Nk, Hkv, d), gen, dev, outlier_frac, outlier_scale)
+    if channel_outliers > 0:
+        cgen = torch.Generator().manual_seed(int(seed) + 11)
+        mult = _channel_mult(Hkv, d, cgen, channel_outliers, channel_scale).to(dev)
+        q = q * mult.repeat_interleave(Hq // Hkv, dim=0)
+        k = k * mult
+    return q.to(dtype), k.to(dtype), v.to(dtype)
 
 
 def hadamard_signs(G, d, seed=0) -> torch.Tensor:
