@@ -41,6 +41,8 @@ WORKLOADS = {
     "bf16_causal_gqa_B1_Hq64_Hkv8_N131072_d128": (1, 64, 8, 131072, 131072, 128, True, "bf16"),
     "fp8_e4m3_B4_H16_N4096_d128": (4, 16, 16, 4096, 4096, 128, False, "fp8"),
     "fp8_e4m3_hadamard_B4_H16_N4096_d128": (4, 16, 16, 4096, 4096, 128, False, "fp8h"),
+    # rotary embedding fused into the Q / K prep (tables built once, outside the steps)
+    "fp8_e4m3_rope_hadamard_B4_H16_N4096_d128": (4, 16, 16, 4096, 4096, 128, False, "fp8hr"),
     # one query per head against a long key cache: split key ranges + LSE merge
     "bf16_decode_splitkv_B1_Hq64_Hkv8_Nq1_Nk131072_d128": (1, 64, 8, 1, 131072, 128, False,
                                                           "decode"),
@@ -286,7 +288,10 @@ def config_of(wl):
             "causal": causal, "scale": "1/sqrt(d)", "parallelism": "replicas",
             "l2": "inputs larger than L2 (Q+K+V+O > 129 MB), no flush between steps",
             "inputs": "iid N(0,1) BSHD, seed 0" + (", 0.1% outliers x50"
-                                                  if kind.startswith("fp8") else "")}
+                                                  if kind.startswith("fp8") else ""),
+            "prep": {"fp8": "per-block E4M3", "fp8h": "Hadamard + per-block E4M3",
+                     "fp8hr": "rotary (rotate-half, base 10000) + Hadamard + per-block E4M3 "
+                              "on Q and K in one pass"}.get(kind, "none")}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -357,8 +362,13 @@ def make_step(wl, dev):
         meta["launches_per_step"] = 1
         return step, e2e, meta
 
-    had = kind == "fp8h"
+    had = kind in ("fp8h", "fp8hr")
+    rope = kind == "fp8hr"
     signs = synth.hadamard_signs(Hkv, d, seed=0).to(dev) if had else None
+    if rope:
+        # one table for Q and K (Nq == Nk here), built on the device once
+        assert Nq == Nk
+        rcos, rsin = attn.attn_rope_table(Nk, d, device=dev)
     npad = (Nk + 15) // 16 * 16
     q8 = torch.empty((B, Nq, Hq, d), dtype=torch.uint8, device=dev)
     k8 = torch.empty((B, Nk, Hkv, d), dtype=torch.uint8, device=dev)
@@ -373,8 +383,12 @@ def make_step(wl, dev):
         if kernel_events:
             pe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             pe[0].record()
-        attn.attn_prep_fp8(q, signs, Hkv if had else None, False, out=q8, descale=qd)
-        attn.attn_prep_fp8(k, signs, Hkv if had else None, False, out=k8, descale=kd)
+        if rope:
+            attn.attn_prep_fp8_rope(q, rcos, rsin, signs, Hkv, out=q8, descale=qd)
+            attn.attn_prep_fp8_rope(k, rcos, rsin, signs, Hkv, out=k8, descale=kd)
+        else:
+            attn.attn_prep_fp8(q, signs, Hkv if had else None, False, out=q8, descale=qd)
+            attn.attn_prep_fp8(k, signs, Hkv if had else None, False, out=k8, descale=kd)
         attn.attn_prep_fp8(v, None, None, True, out=v8, descale=vd)
         if kernel_events:
             pe[1].record()
@@ -398,6 +412,9 @@ def make_step(wl, dev):
     meta["prep_events"] = prep_ev
     # prep: every bf16 element read once, one E4M3 byte written, one descale per block
     meta["prep_bytes"] = sum(t.numel() * 3 for t in (q, k, v)) + 4 * (qd.numel() + 2 * kd.numel())
+    if rope:
+        # the cos / sin tables, read once for Q and once for K
+        meta["prep_bytes"] += 2 * (rcos.numel() + rsin.numel()) * 4
     return step, e2e, meta
 
 

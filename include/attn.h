@@ -121,6 +121,73 @@ int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int64_t
                   const int8_t* signs, int sign_heads, int transpose_out, void* stream);
 
 /*
+ * attn_prep_fp8_per_tensor - the baseline FP8 scheme: one scale for the
+ * whole tensor instead of one per block, optional Hadamard transform.
+ *
+ * The summary card (FlashAttention-3 summary, low-precision section) says
+ * incoherent processing makes the FP8 error 2.6 times lower than "baseline
+ * FP8" without defining it; this is the reading taken for that baseline.
+ *
+ *   x, x8, signs, sign_heads, transpose_out, d: as attn_prep_fp8.
+ *   descale  [B, H, ceil(N/128)] float32 (written): every entry equals
+ *            amax / 448 with amax over the whole tensor after the transform
+ *            (1 for an all-zero tensor), so attn_fwd_fp8 consumes it
+ *            unchanged.  code = E4M3_RNE_satfinite(y * r), r = 448 / amax
+ *            rounded to float32 once.  descale[0] serves as the amax
+ *            accumulator while the call runs (three kernels and a 4-byte
+ *            memset on `stream`).
+ *   Returns as attn_prep_fp8.
+ */
+int attn_prep_fp8_per_tensor(const void* x, void* x8, float* descale, int B, int H, int64_t N,
+                             int d, const int8_t* signs, int sign_heads, int transpose_out,
+                             void* stream);
+
+/*
+ * attn_rope_table - cos and sin tables of the rotary embedding, for
+ * attn_prep_fp8_rope.
+ *
+ * The pages name no rotary variant; the one taken is the rotate-half form:
+ * channel c < d/2 pairs with c + d/2 and both turn by the angle
+ * (pos0 + n) * base^(-2c/d) at token n.
+ *
+ *   rope_cos, rope_sin  [N, d/2] float32 (device, written, caller-owned):
+ *            cos and sin of the angle, evaluated in double precision and
+ *            rounded once to float32.
+ *   N        positions (0 returns ATTN_OK with nothing written)
+ *   d        even, 2..256
+ *   base     > 1 (10000 in most models)
+ *   pos0     position of the first row, 0..2^40
+ *   Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_MISALIGNED (tables not
+ *   4-byte aligned) or ATTN_ERR_CUDA.
+ */
+int attn_rope_table(float* rope_cos, float* rope_sin, int64_t N, int d, double base,
+                    int64_t pos0, void* stream);
+
+/*
+ * attn_prep_fp8_rope - rotary embedding, optional Hadamard transform and
+ * per-block FP8 quantisation in one pass over a Q or K tensor.
+ *
+ * The summary card (FlashAttention-3 summary, low-precision section) notes
+ * that the Hadamard transform can be fused with the rotary embedding, a
+ * bandwidth-bound step, at no extra cost.  Each row is rotated (rotate-half
+ * form, see attn_rope_table) in float32, then transformed as in
+ * attn_prep_fp8 (when signs is not NULL), then quantised per block.  The
+ * rotation is applied before the transform so that the scores are those of
+ * the rotated Q and K.
+ *
+ *   x        [B, N, H, d] bfloat16 (read)
+ *   x8       [B, N, H, d] E4M3 codes (written; BSHD only - V takes no rotation)
+ *   descale  [B, H, ceil(N/128)] float32 (written), as attn_prep_fp8
+ *   rope_cos, rope_sin  [N, d/2] float32 (read; attn_rope_table), row n
+ *            for token n of every batch; 16-byte aligned
+ *   signs, sign_heads, d: as attn_prep_fp8
+ *   Returns as attn_prep_fp8; ATTN_ERR_INVALID_ARG for a NULL table.
+ */
+int attn_prep_fp8_rope(const void* x, void* x8, float* descale, int B, int H, int64_t N, int d,
+                       const float* rope_cos, const float* rope_sin, const int8_t* signs,
+                       int sign_heads, void* stream);
+
+/*
  * attn_fwd_fp8 - fused attention forward on FP8 E4M3 inputs.
  *
  *   q8        [B, Nq, Hq, d]     E4M3 codes       q_descale [B, Hq, ceil(Nq/128)]

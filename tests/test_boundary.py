@@ -95,6 +95,26 @@ def test_fp8_and_prep_reject_bad_arguments_on_host(lib):
     assert L.attn_fwd_fp8(*bad) == attn.ERR_MISALIGNED
 
 
+def test_prep_variants_reject_bad_arguments_on_host(lib):
+    L = lib
+    # per-tensor: same checks as the per-block prep
+    assert L.attn_prep_fp8_per_tensor(A, A, A, 1, 4, 100, 96, None, 0, 0, None) == attn.ERR_UNSUPPORTED
+    assert L.attn_prep_fp8_per_tensor(A, A, A, 1, 4, 100, 128, A, 3, 0, None) == attn.ERR_INVALID_ARG
+    assert L.attn_prep_fp8_per_tensor(A, A + 8, A, 1, 4, 100, 128, None, 0, 0, None) == attn.ERR_MISALIGNED
+    assert L.attn_prep_fp8_per_tensor(A, A, A, 1, 4, 0, 128, None, 0, 0, None) == attn.OK
+    # rotary prep: tables required and 16-byte aligned
+    assert L.attn_prep_fp8_rope(A, A, A, 1, 4, 100, 128, None, A, None, 0, None) == attn.ERR_INVALID_ARG
+    assert L.attn_prep_fp8_rope(A, A, A, 1, 4, 100, 128, A + 4, A, None, 0, None) == attn.ERR_MISALIGNED
+    assert L.attn_prep_fp8_rope(A, A, A, 1, 4, 100, 100, A, A, None, 0, None) == attn.ERR_UNSUPPORTED
+    assert L.attn_prep_fp8_rope(A, A, A, 0, 4, 100, 128, None, None, None, 0, None) == attn.OK
+    # tables: odd or too large d, base <= 1, negative offset, empty
+    assert L.attn_rope_table(A, A, 10, 7, 10000.0, 0, None) == attn.ERR_INVALID_ARG
+    assert L.attn_rope_table(A, A, 10, 512, 10000.0, 0, None) == attn.ERR_INVALID_ARG
+    assert L.attn_rope_table(A, A, 10, 128, 1.0, 0, None) == attn.ERR_INVALID_ARG
+    assert L.attn_rope_table(A, A, 10, 128, 10000.0, -1, None) == attn.ERR_INVALID_ARG
+    assert L.attn_rope_table(A, A, 0, 128, 10000.0, 0, None) == attn.OK
+
+
 def test_strerror_covers_every_code(lib):
     for c in (attn.OK, attn.ERR_INVALID_ARG, attn.ERR_UNSUPPORTED, attn.ERR_MISALIGNED,
               attn.ERR_CUDA, attn.ERR_TIMEOUT, attn.ERR_DEVICE):

@@ -1,5 +1,6 @@
 """GPU parity of the FP8 path: the prep kernel (per-block E4M3 quantisation,
-optional Hadamard transform) and the FP8 fused forward.
+optional Hadamard transform; the per-tensor baseline; the fused rotary
+variant and its tables) and the FP8 fused forward.
 
 * Prep without the transform: the quantised values are exact float32
   quotients on both sides, so codes and descales must match the oracle bit
@@ -86,13 +87,14 @@ def _fp8_forward(gpu_lib, q, k, v, causal, hadamard, Hkv):
     return o, lse
 
 
-def _oracle_dequant(q, k, v, causal, hadamard, Hkv, rows=None):
+def _oracle_dequant(q, k, v, causal, hadamard, Hkv, rows=None, per_tensor=False, rope=False):
     """Oracle on its own FP8 quantisation of the same inputs (dequantised)."""
     d = q.shape[-1]
     sg = synth.hadamard_signs(Hkv, d, seed=0).numpy() if hadamard else None
     deq = []
-    for t, had in ((q, hadamard), (k, hadamard), (v, False)):
-        c, ds, _ = ofp8.prepare(t.double().cpu().numpy(), sg, had)
+    for t, had, rot in ((q, hadamard, rope), (k, hadamard, rope), (v, False, False)):
+        c, ds, _ = ofp8.prepare(t.double().cpu().numpy(), sg, had, per_tensor=per_tensor,
+                                rope_base=10000.0 if rot else None)
         deq.append(ofp8.dequantize(c, ds))
     qd, kd, vd = deq
     scale = 1 / math.sqrt(d)
@@ -160,3 +162,123 @@ def test_fp8_full_workload_accuracy_and_hadamard(gpu_lib, outlier_scale):
     assert rms[True] <= rms[False], rms
     if outlier_scale <= 10.0:
         assert rms[False] <= 5e-2 and rms[True] <= 5e-2, rms
+
+
+# --- per-tensor baseline ------------------------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_prep_per_tensor_bit_exact_without_transform(gpu_lib, d):
+    B, N, H = 2, 1000, 3
+    x, _, _ = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=21,
+                                outlier_frac=1e-3)
+    codes, ds = gpu_lib.attn_prep_fp8_per_tensor(x.cuda())
+    codes_t, ds_t = gpu_lib.attn_prep_fp8_per_tensor(x.cuda(), transpose_out=True)
+    assert gpu_lib.get_status() == 0
+    oc, ods, _ = ofp8.prepare(x.float().numpy(), per_tensor=True)
+    np.testing.assert_array_equal(ds.cpu().numpy(), ods)
+    np.testing.assert_array_equal(ds_t.cpu().numpy(), ods)
+    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    np.testing.assert_array_equal(codes_t.cpu().numpy()[..., :N], oc.transpose(0, 2, 3, 1))
+    # a second call on other data leaves nothing behind (descale[0] is reused
+    # as the amax accumulator)
+    z = torch.zeros_like(x).cuda()
+    cz, dz = gpu_lib.attn_prep_fp8_per_tensor(z, descale=ds)
+    assert not cz.any() and bool((dz == 1.0).all())
+
+
+def _codes_near(g, q_exact, rel=4e-6, abs_=4e-5):
+    """Every code is the E4M3 code of a value within the tolerance of the
+    exact scaled value; almost all are the exact nearest-even code."""
+    tol = rel * np.abs(q_exact) + abs_
+    lo, hi = ofp8.e4m3_encode(q_exact - tol), ofp8.e4m3_encode(q_exact + tol)
+    ok = (g == lo) | (g == hi)
+    assert ok.all(), np.argwhere(~ok)[:5]
+    assert np.mean(g != ofp8.e4m3_encode(q_exact)) < 1e-3
+
+
+def test_prep_per_tensor_with_transform(gpu_lib):
+    B, N, Hq, Hkv, d = 1, 700, 4, 2, 128
+    x, _, _ = synth.attn_inputs(B, N, N, Hq, Hkv, d, dtype=torch.bfloat16, seed=22,
+                                outlier_frac=1e-3)
+    signs = _signs(Hkv, d)
+    codes, ds = gpu_lib.attn_prep_fp8_per_tensor(x.cuda(), signs=signs, sign_heads=Hkv)
+    assert gpu_lib.get_status() == 0
+    y64 = ofp8.incoherent_transform(x.double().numpy(), signs.cpu().numpy())
+    _, ods, _ = ofp8.prepare(x.double().numpy(), signs.cpu().numpy(), True, per_tensor=True)
+    g_ds = ds.cpu().numpy()
+    np.testing.assert_allclose(g_ds, ods, rtol=4e-6, atol=0)
+    assert np.all(g_ds == g_ds.flat[0])
+    _codes_near(codes.cpu().numpy(), y64 / float(g_ds.flat[0]))
+
+
+# --- rotary embedding fused into the prep -------------------------------------
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("pos0", [0, 123457])
+def test_rope_table_matches_oracle(gpu_lib, d, pos0):
+    N = 3000
+    cos, sin = gpu_lib.attn_rope_table(N, d, base=10000.0, pos0=pos0)
+    assert gpu_lib.get_status() == 0
+    oc, osn = ofp8.rope_tables(N, d, 10000.0, pos0)
+    # double-precision evaluation rounded once to float32: within half a
+    # float32 ulp of 1 (plus the double evaluation's own error)
+    np.testing.assert_allclose(cos.cpu().numpy(), oc, rtol=0, atol=7e-8)
+    np.testing.assert_allclose(sin.cpu().numpy(), osn, rtol=0, atol=7e-8)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_prep_rope_matches_oracle(gpu_lib, d, hadamard):
+    """Rotation, transform and block quantisation in one pass, against the
+    oracle's float64 rotation (and transform) of the same rows: codes within
+    the float32 rounding of the exact scaled value, descales to float32
+    rounding; ragged last block."""
+    B, N, Hq, Hkv = 2, 650, 4, 2
+    x, _, _ = synth.attn_inputs(B, N, N, Hq, Hkv, d, dtype=torch.bfloat16, seed=23,
+                                outlier_frac=1e-3)
+    cos, sin = gpu_lib.attn_rope_table(N, d)
+    signs = _signs(Hkv, d) if hadamard else None
+    codes, ds = gpu_lib.attn_prep_fp8_rope(x.cuda(), cos, sin, signs=signs,
+                                           sign_heads=Hkv if hadamard else None)
+    assert gpu_lib.get_status() == 0
+    y64 = ofp8.rope(x.double().numpy(), 10000.0)
+    if hadamard:
+        y64 = ofp8.incoherent_transform(y64, signs.cpu().numpy())
+    _, ods, _ = ofp8.prepare(x.double().numpy(), signs.cpu().numpy() if hadamard else None,
+                             hadamard, rope_base=10000.0)
+    g_ds = ds.cpu().numpy()
+    np.testing.assert_allclose(g_ds, ods, rtol=4e-6, atol=0)
+    t = np.arange(N) // 128
+    q_exact = y64 / g_ds.astype(np.float64)[:, :, t].transpose(0, 2, 1)[..., None]
+    _codes_near(codes.cpu().numpy(), q_exact)
+
+
+@pytest.mark.parametrize("variant", ["per_tensor", "per_tensor_hadamard", "rope", "rope_hadamard"])
+def test_fp8_forward_variants_vs_dequantised_oracle(gpu_lib, variant):
+    """The forward on per-tensor and on rotated codes, every row, against the
+    oracle run on its own dequantised quantisation of the same inputs."""
+    B, N, Hq, Hkv, d = 1, 700, 4, 2, 128
+    q, k, v = synth.attn_inputs(B, N, N, Hq, Hkv, d, dtype=torch.bfloat16, seed=24,
+                                outlier_frac=1e-3, outlier_scale=10.0, device="cuda")
+    had = variant.endswith("hadamard")
+    signs = _signs(Hkv, d) if had else None
+    sh = Hkv if had else None
+    if variant.startswith("per_tensor"):
+        q8, qd = gpu_lib.attn_prep_fp8_per_tensor(q, signs=signs, sign_heads=sh)
+        k8, kd = gpu_lib.attn_prep_fp8_per_tensor(k, signs=signs, sign_heads=sh)
+        v8, vd = gpu_lib.attn_prep_fp8_per_tensor(v, transpose_out=True)
+    else:
+        cos, sin = gpu_lib.attn_rope_table(N, d)
+        q8, qd = gpu_lib.attn_prep_fp8_rope(q, cos, sin, signs=signs, sign_heads=sh)
+        k8, kd = gpu_lib.attn_prep_fp8_rope(k, cos, sin, signs=signs, sign_heads=sh)
+        v8, vd = gpu_lib.attn_prep_fp8(v, transpose_out=True)
+    o, lse = gpu_lib.attn_fwd_fp8(q8, k8, v8, qd, kd, vd, causal=True, hadamard=had)
+    assert gpu_lib.get_status() == 0
+    o_ref, lse_ref = _oracle_dequant(q, k, v, True, had, Hkv,
+                                     per_tensor=variant.startswith("per_tensor"),
+                                     rope=variant.startswith("rope"))
+    e = errors(o, lse, o_ref, lse_ref)
+    assert e["nonfinite"] == 0, e
+    assert e["o_rel_rms"] <= 4e-2, e
+    exact_codes = variant == "per_tensor"
+    assert e["lse_max_abs"] <= (2e-3 if exact_codes else 1e-2), e

@@ -25,7 +25,8 @@ ERR_SCRATCH = -7
 
 EXPORTS = ("attn_fwd", "attn_prep_fp8", "attn_fwd_fp8", "attn_get_status", "attn_strerror",
            "attn_launch_count", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
-           "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc")
+           "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_prep_fp8_per_tensor",
+           "attn_rope_table", "attn_prep_fp8_rope")
 
 _lib = None
 
@@ -69,6 +70,12 @@ def load():
                                              f32, i32, vp]
     lib.attn_splitkv_default_splits.restype = i32
     lib.attn_splitkv_default_splits.argtypes = [i32, i32, i32, i64, i64, i32]
+    lib.attn_prep_fp8_per_tensor.restype = i32
+    lib.attn_prep_fp8_per_tensor.argtypes = [vp, vp, vp, i32, i32, i64, i32, vp, i32, i32, vp]
+    lib.attn_rope_table.restype = i32
+    lib.attn_rope_table.argtypes = [vp, vp, i64, i32, ctypes.c_double, i64, vp]
+    lib.attn_prep_fp8_rope.restype = i32
+    lib.attn_prep_fp8_rope.argtypes = [vp, vp, vp, i32, i32, i64, i32, vp, vp, vp, i32, vp]
     _lib = lib
     return lib
 
@@ -173,13 +180,7 @@ def attn_fwd_splitkv(q, k, v, num_splits: int | None = None, scale: float | None
     return out, lse
 
 
-def attn_prep_fp8(x, signs=None, sign_heads: int | None = None, transpose_out: bool = False,
-                  out=None, descale=None, stream=None):
-    """Per-128-token-block E4M3 quantisation of x [B, N, H, d] (bf16), with the
-    optional Hadamard transform (signs [G, d] int8 +-1 on the device).
-    Returns (codes uint8, descale fp32 [B, H, ceil(N/128)]); codes are
-    [B, N, H, d], or [B, H, d, Npad] (Npad = N rounded up to 16) when
-    ``transpose_out``."""
+def _prep_buffers(x, signs, sign_heads, transpose_out, out, descale):
     _need_cuda(x)
     if x.dtype != torch.bfloat16:
         raise ValueError("x must be bfloat16")
@@ -199,9 +200,66 @@ def attn_prep_fp8(x, signs=None, sign_heads: int | None = None, transpose_out: b
         if signs.dtype != torch.int8 or signs.shape[1] != d:
             raise ValueError("signs must be int8 [G, d]")
         sign_heads = signs.shape[0] if sign_heads is None else sign_heads
-    rc = load().attn_prep_fp8(_ptr(x), _ptr(out), _ptr(descale), B, H, N, d, _ptr(signs),
-                              int(sign_heads or 0), int(bool(transpose_out)), _stream(stream))
+    return out, descale, int(sign_heads or 0)
+
+
+def attn_prep_fp8(x, signs=None, sign_heads: int | None = None, transpose_out: bool = False,
+                  out=None, descale=None, stream=None):
+    """Per-128-token-block E4M3 quantisation of x [B, N, H, d] (bf16), with the
+    optional Hadamard transform (signs [G, d] int8 +-1 on the device).
+    Returns (codes uint8, descale fp32 [B, H, ceil(N/128)]); codes are
+    [B, N, H, d], or [B, H, d, Npad] (Npad = N rounded up to 16) when
+    ``transpose_out``."""
+    out, descale, sh = _prep_buffers(x, signs, sign_heads, transpose_out, out, descale)
+    B, N, H, d = x.shape
+    rc = load().attn_prep_fp8(_ptr(x), _ptr(out), _ptr(descale), B, H, N, d, _ptr(signs), sh,
+                              int(bool(transpose_out)), _stream(stream))
     _check(rc, "attn_prep_fp8")
+    return out, descale
+
+
+def attn_prep_fp8_per_tensor(x, signs=None, sign_heads: int | None = None,
+                             transpose_out: bool = False, out=None, descale=None, stream=None):
+    """One E4M3 scale for the whole tensor (the baseline FP8 scheme); same
+    arguments and outputs as attn_prep_fp8, every descale entry equal."""
+    out, descale, sh = _prep_buffers(x, signs, sign_heads, transpose_out, out, descale)
+    B, N, H, d = x.shape
+    rc = load().attn_prep_fp8_per_tensor(_ptr(x), _ptr(out), _ptr(descale), B, H, N, d,
+                                         _ptr(signs), sh, int(bool(transpose_out)),
+                                         _stream(stream))
+    _check(rc, "attn_prep_fp8_per_tensor")
+    return out, descale
+
+
+def attn_rope_table(N: int, d: int, base: float = 10000.0, pos0: int = 0, device="cuda",
+                    stream=None):
+    """cos, sin float32 [N, d/2] of the rotate-half rotary angles
+    (pos0 + n) * base^(-2c/d), computed on the device."""
+    cos = torch.empty((N, d // 2), dtype=torch.float32, device=device)
+    sin = torch.empty((N, d // 2), dtype=torch.float32, device=device)
+    _need_cuda(cos)
+    rc = load().attn_rope_table(_ptr(cos), _ptr(sin), int(N), int(d), float(base), int(pos0),
+                                _stream(stream))
+    _check(rc, "attn_rope_table")
+    return cos, sin
+
+
+def attn_prep_fp8_rope(x, rope_cos, rope_sin, signs=None, sign_heads: int | None = None,
+                       out=None, descale=None, stream=None):
+    """Rotary embedding (tables from attn_rope_table, [N, d/2] float32), then
+    the optional Hadamard transform, then per-block E4M3 quantisation of a Q
+    or K tensor x [B, N, H, d] (bf16).  Returns (codes [B, N, H, d], descale)."""
+    out, descale, sh = _prep_buffers(x, signs, sign_heads, False, out, descale)
+    B, N, H, d = x.shape
+    _need_cuda(rope_cos, rope_sin)
+    if (rope_cos.dtype != torch.float32 or rope_sin.dtype != torch.float32
+            or tuple(rope_cos.shape) != (N, d // 2) or tuple(rope_sin.shape) != (N, d // 2)
+            or not rope_cos.is_contiguous() or not rope_sin.is_contiguous()):
+        raise ValueError("rope tables must be contiguous float32 [N, d/2]")
+    rc = load().attn_prep_fp8_rope(_ptr(x), _ptr(out), _ptr(descale), B, H, N, d,
+                                   _ptr(rope_cos), _ptr(rope_sin), _ptr(signs), sh,
+                                   _stream(stream))
+    _check(rc, "attn_prep_fp8_rope")
     return out, descale
 
 

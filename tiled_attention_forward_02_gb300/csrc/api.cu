@@ -235,9 +235,10 @@ extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
   return launch_fwd_e4m3(d, causal, mq, mk, mv, p, grid, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int64_t N,
-                             int d, const int8_t* signs, int sign_heads, int transpose_out,
-                             void* stream) {
+namespace {
+// argument checks shared by the prep variants
+int check_prep(const void* x, const void* x8, const float* descale, int B, int H, int64_t N,
+               int d, const int8_t* signs, int sign_heads, int transpose_out) {
   if (B < 0 || H < 1 || N < 0) return ATTN_ERR_INVALID_ARG;
   if (transpose_out != 0 && transpose_out != 1) return ATTN_ERR_INVALID_ARG;
   if (signs && (sign_heads < 1 || H % sign_heads != 0)) return ATTN_ERR_INVALID_ARG;
@@ -247,11 +248,60 @@ extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int
   if (B == 0 || N == 0) return ATTN_OK;
   if (!x || !x8 || !descale) return ATTN_ERR_INVALID_ARG;
   if (!aligned(x, 128) || !aligned(x8, 128) || !aligned(descale, 16)) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+}  // namespace
+
+extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int64_t N,
+                             int d, const int8_t* signs, int sign_heads, int transpose_out,
+                             void* stream) {
+  int rc = check_prep(x, x8, descale, B, H, N, d, signs, sign_heads, transpose_out);
+  if (rc != ATTN_OK || B == 0 || N == 0) return rc;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  const int group = signs ? H / sign_heads : 1;
+  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
+                         nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_prep_fp8_per_tensor(const void* x, void* x8, float* descale, int B, int H,
+                                        int64_t N, int d, const int8_t* signs, int sign_heads,
+                                        int transpose_out, void* stream) {
+  int rc = check_prep(x, x8, descale, B, H, N, d, signs, sign_heads, transpose_out);
+  if (rc != ATTN_OK || B == 0 || N == 0) return rc;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  const int group = signs ? H / sign_heads : 1;
+  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
+                         nullptr, 1, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_rope_table(float* rope_cos, float* rope_sin, int64_t N, int d, double base,
+                               int64_t pos0, void* stream) {
+  if (N < 0 || N > kMaxRows || d < 2 || d > 256 || (d & 1)) return ATTN_ERR_INVALID_ARG;
+  if (!(base > 1.0) || !isfinite(base) || pos0 < 0 || pos0 > ((int64_t)1 << 40))
+    return ATTN_ERR_INVALID_ARG;
+  if (N == 0) return ATTN_OK;
+  if (!rope_cos || !rope_sin) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(rope_cos, 4) || !aligned(rope_sin, 4)) return ATTN_ERR_MISALIGNED;
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc != ATTN_OK) return rc;
+  return launch_rope_table(rope_cos, rope_sin, (int)N, d, base, (long long)pos0,
+                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_prep_fp8_rope(const void* x, void* x8, float* descale, int B, int H,
+                                  int64_t N, int d, const float* rope_cos, const float* rope_sin,
+                                  const int8_t* signs, int sign_heads, void* stream) {
+  int rc = check_prep(x, x8, descale, B, H, N, d, signs, sign_heads, 0);
+  if (rc != ATTN_OK || B == 0 || N == 0) return rc;
+  if (!rope_cos || !rope_sin) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(rope_cos, 16) || !aligned(rope_sin, 16)) return ATTN_ERR_MISALIGNED;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != ATTN_OK) return rc;
   const int group = signs ? H / sign_heads : 1;
-  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, transpose_out,
+  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, 0, rope_cos, rope_sin, 0,
                          static_cast<cudaStream_t>(stream));
 }
 

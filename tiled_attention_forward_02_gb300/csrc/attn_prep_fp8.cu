@@ -17,6 +17,17 @@
 // saturated to +-448 by the hardware conversion; descale = amax / 448.  The
 // kernel is bandwidth-bound: it reads each bf16 element once and writes one
 // byte per element.
+//
+// Two variants share the kernel:
+// * rotary embedding before the transform (the summary card notes that the
+//   transform can ride along with the rotary embedding, a bandwidth-bound
+//   step): rotate-half form, channel c paired with c + d/2; the pair sits in
+//   lanes hl and hl ^ 8 of the half warp, one shuffle per value; cos and sin
+//   come from float32 tables [N, d/2] (attn_rope_table);
+// * one scale per tensor (the baseline FP8 scheme): a first pass only
+//   reduces the tensor's amax (atomic max of the float bits, all values >= 0),
+//   a second quantises every block with that amax, and a one-CTA kernel
+//   writes the descale of every block.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -48,13 +59,32 @@ __device__ __forceinline__ void load_row_part(const uint16_t* src, float (&y)[D 
   }
 }
 
-template <int D>
+// quantisation modes
+enum PrepMode : int {
+  kPrepBlock = 0,       // scale per 128-token block (writes codes and descales)
+  kPrepTensorAmax = 1,  // per-tensor, first pass: amax only
+  kPrepTensor = 2,      // per-tensor, second pass: codes from the tensor amax
+};
+
+template <int VEC>
+__device__ __forceinline__ void load_f32(const float* src, float (&t)[VEC]) {
+#pragma unroll
+  for (int q = 0; q < VEC / 4; ++q) {
+    const float4 w = __ldg(reinterpret_cast<const float4*>(src) + q);
+    t[4 * q] = w.x; t[4 * q + 1] = w.y; t[4 * q + 2] = w.z; t[4 * q + 3] = w.w;
+  }
+}
+
+template <int D, int MODE, bool ROPE>
 __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restrict__ x,
                                                        uint8_t* __restrict__ x8,
                                                        float* __restrict__ descale,
                                                        const int8_t* __restrict__ signs,
                                                        int sign_group, int H, int N, int nb,
-                                                       int Npad, int transpose_out) {
+                                                       int Npad, int transpose_out,
+                                                       const float* __restrict__ rope_cos,
+                                                       const float* __restrict__ rope_sin,
+                                                       float* tensor_amax) {
   constexpr int VEC = D / 16;  // elements per lane (a half warp covers one row)
   constexpr int ITERS = 8;     // 8 warps x 2 rows x 8 iterations = 128 rows
   __shared__ float s_amax[8];
@@ -89,6 +119,27 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restric
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < ITERS; ++i) {
+    if constexpr (ROPE) {
+      // (y_c, y_{c+D/2}) -> (y_c cos - y_{c+D/2} sin, y_{c+D/2} cos + y_c sin);
+      // lane hl holds channels hl*VEC.., its partner lane hl ^ 8
+      const int n = row_of(i);
+      float cs[VEC], sn[VEC];
+      if (n < N) {
+        const long long off = (long long)n * (D / 2) + (hl & 7) * VEC;
+        load_f32<VEC>(rope_cos + off, cs);
+        load_f32<VEC>(rope_sin + off, sn);
+      } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) { cs[v] = 1.f; sn[v] = 0.f; }
+      }
+      const bool upper = hl >= 8;
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) {
+        const float other = __shfl_xor_sync(0xffffffffu, y[i][v], 8);
+        const float t = upper ? other * sn[v] : -(other * sn[v]);
+        y[i][v] = fmaf(y[i][v], cs[v], t);
+      }
+    }
     if (signs) {
 #pragma unroll
       for (int v = 0; v < VEC; ++v) y[i][v] *= sg[v];
@@ -122,17 +173,29 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restric
     for (int v = 0; v < VEC; ++v) amax = fmaxf(amax, fabsf(y[i][v]));
   }
 
+  float bmax;
+  if constexpr (MODE == kPrepTensor) {
+    bmax = *tensor_amax;   // written by the amax pass, read-only here
+  } else {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if (lane == 0) s_amax[warp] = amax;
-  __syncthreads();
-  float bmax = s_amax[0];
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) s_amax[warp] = amax;
+    __syncthreads();
+    bmax = s_amax[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, s_amax[w]);
-  const float ds = bmax > 0.f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
+    for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, s_amax[w]);
+  }
+  if constexpr (MODE == kPrepTensorAmax) {
+    // non-negative floats order like their bit patterns
+    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(tensor_amax), __float_as_uint(bmax));
+    return;
+  }
   // codes are y * (448 / amax), the reciprocal taken once per block
   const float inv_ds = bmax > 0.f ? __fdiv_rn(448.0f, bmax) : 1.0f;
-  if (threadIdx.x == 0) descale[((long long)b * H + h) * nb + blk] = ds;
+  if constexpr (MODE == kPrepBlock) {
+    const float ds = bmax > 0.f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
+    if (threadIdx.x == 0) descale[((long long)b * H + h) * nb + blk] = ds;
+  }
 
 #pragma unroll
   for (int i = 0; i < ITERS; ++i) {
@@ -178,29 +241,106 @@ __global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restric
   }
 }
 
+// descale of every block from the tensor amax in descale[0]; one CTA, every
+// thread reads descale[0] before any thread writes
+__global__ void __launch_bounds__(256) prep_fill_descale_kernel(float* descale, long long n) {
+  const float amax = descale[0];
+  __syncthreads();
+  const float ds = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) descale[i] = ds;
+}
+
+// cos / sin of angle (pos0 + n) * base^(-2c/d), computed in double and
+// rounded once to float32; one CTA per 64 positions
+__global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cos_out,
+                                                         float* __restrict__ sin_out, int N,
+                                                         int d, double base, long long pos0) {
+  __shared__ double s_freq[128];
+  const int half = d / 2;
+  for (int c = threadIdx.x; c < half; c += blockDim.x) s_freq[c] = pow(base, -2.0 * c / d);
+  __syncthreads();
+  const long long n0 = (long long)blockIdx.x * 64;
+  for (int t = threadIdx.x; t < 64 * half; t += blockDim.x) {
+    const long long n = n0 + t / half;
+    const int c = t % half;
+    if (n >= N) break;
+    double sv, cv;
+    sincos((double)(pos0 + n) * s_freq[c], &sv, &cv);
+    cos_out[n * half + c] = (float)cv;
+    sin_out[n * half + c] = (float)sv;
+  }
+}
+
+template <int D, int MODE, bool ROPE>
+void launch_prep_instance(dim3 grid, cudaStream_t stream, const uint16_t* xs, uint8_t* xo,
+                          float* descale, const int8_t* signs, int sign_group, int H, int N,
+                          int nb, int Npad, int transpose_out, const float* rc, const float* rs,
+                          float* tamax) {
+  prep_fp8_kernel<D, MODE, ROPE><<<grid, 256, 0, stream>>>(
+      xs, xo, descale, signs, sign_group, H, N, nb, Npad, transpose_out, rc, rs, tamax);
+}
+
+template <int MODE, bool ROPE>
+int launch_prep_d(int d, dim3 grid, cudaStream_t stream, const uint16_t* xs, uint8_t* xo,
+                  float* descale, const int8_t* signs, int sign_group, int H, int N, int nb,
+                  int Npad, int transpose_out, const float* rc, const float* rs, float* tamax) {
+  switch (d) {
+    case 64:
+      launch_prep_instance<64, MODE, ROPE>(grid, stream, xs, xo, descale, signs, sign_group, H,
+                                           N, nb, Npad, transpose_out, rc, rs, tamax);
+      break;
+    case 128:
+      launch_prep_instance<128, MODE, ROPE>(grid, stream, xs, xo, descale, signs, sign_group, H,
+                                            N, nb, Npad, transpose_out, rc, rs, tamax);
+      break;
+    case 256:
+      launch_prep_instance<256, MODE, ROPE>(grid, stream, xs, xo, descale, signs, sign_group, H,
+                                            N, nb, Npad, transpose_out, rc, rs, tamax);
+      break;
+    default:
+      return ATTN_ERR_UNSUPPORTED;
+  }
+  note_launch();
+  return check_launch();
+}
+
 int launch_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int N, int d,
-                    const int8_t* signs, int sign_group, int transpose_out, cudaStream_t stream) {
+                    const int8_t* signs, int sign_group, int transpose_out, const float* rope_cos,
+                    const float* rope_sin, int per_tensor, cudaStream_t stream) {
   const int nb = (N + 127) / 128;
   const int Npad = (N + 15) / 16 * 16;
   dim3 grid(H, nb, B);
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint8_t* xo = static_cast<uint8_t*>(x8);
-  switch (d) {
-    case 64:
-      prep_fp8_kernel<64><<<grid, 256, 0, stream>>>(xs, xo, descale, signs, sign_group, H, N, nb,
-                                                    Npad, transpose_out);
-      break;
-    case 128:
-      prep_fp8_kernel<128><<<grid, 256, 0, stream>>>(xs, xo, descale, signs, sign_group, H, N, nb,
-                                                     Npad, transpose_out);
-      break;
-    case 256:
-      prep_fp8_kernel<256><<<grid, 256, 0, stream>>>(xs, xo, descale, signs, sign_group, H, N, nb,
-                                                     Npad, transpose_out);
-      break;
-    default:
-      return ATTN_ERR_UNSUPPORTED;
+  if (!per_tensor) {
+    if (rope_cos)
+      return launch_prep_d<kPrepBlock, true>(d, grid, stream, xs, xo, descale, signs, sign_group,
+                                             H, N, nb, Npad, transpose_out, rope_cos, rope_sin,
+                                             nullptr);
+    return launch_prep_d<kPrepBlock, false>(d, grid, stream, xs, xo, descale, signs, sign_group,
+                                            H, N, nb, Npad, transpose_out, nullptr, nullptr,
+                                            nullptr);
   }
+  if (rope_cos) return ATTN_ERR_UNSUPPORTED;
+  // the tensor amax is accumulated in descale[0] and read from there
+  cudaError_t e = cudaMemsetAsync(descale, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(descale)");
+  int rc = launch_prep_d<kPrepTensorAmax, false>(d, grid, stream, xs, xo, descale, signs,
+                                                 sign_group, H, N, nb, Npad, transpose_out,
+                                                 nullptr, nullptr, descale);
+  if (rc != ATTN_OK) return rc;
+  rc = launch_prep_d<kPrepTensor, false>(d, grid, stream, xs, xo, descale, signs, sign_group, H,
+                                         N, nb, Npad, transpose_out, nullptr, nullptr, descale);
+  if (rc != ATTN_OK) return rc;
+  prep_fill_descale_kernel<<<1, 256, 0, stream>>>(descale, (long long)B * H * nb);
+  note_launch();
+  return check_launch();
+}
+
+int launch_rope_table(float* cos_out, float* sin_out, int N, int d, double base, long long pos0,
+                      cudaStream_t stream) {
+  const int blocks = (N + 63) / 64;
+  rope_table_kernel<<<blocks, 256, 0, stream>>>(cos_out, sin_out, N, d, base, pos0);
   note_launch();
   return check_launch();
 }
