@@ -73,10 +73,11 @@ int device_state(DeviceState** out) {
 }
 
 int encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const cuuint64_t dims[4],
-           const cuuint64_t strides[3], const cuuint32_t box[4]) {
+           const cuuint64_t strides[3], const cuuint32_t box[4],
+           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(g_cuda_msg, sizeof(g_cuda_msg), "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
@@ -95,6 +96,17 @@ int map_bshd(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* base
                                  (cuuint64_t)N * H * d * esz};
   const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)heads, (cuuint32_t)(128 / heads), 1};
   return encode(map, dt, base, dims, strides, box);
+}
+
+// prep input [B, N, H, d] bf16 as dims (d, H, N, B); box = one head's 128 rows
+// of d elements, unswizzled (row r of the tile at r * d * 2 bytes)
+int map_prep(CUtensorMap* map, const void* base, int B, int64_t N, int H, int d) {
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2,
+                                 (cuuint64_t)N * H * d * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)d, 1, 128, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // transposed value tensor [B, H, d, Npad] (bytes) as dims (Npad, d, H, B);
@@ -259,9 +271,11 @@ extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int
   if (rc != ATTN_OK || B == 0 || N == 0) return rc;
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  CUtensorMap mx;
+  if ((rc = map_prep(&mx, x, B, N, H, d)) != ATTN_OK) return rc;
   const int group = signs ? H / sign_heads : 1;
-  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
-                         nullptr, 0, static_cast<cudaStream_t>(stream));
+  return launch_prep_fp8(mx, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
+                         nullptr, 0, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_prep_fp8_per_tensor(const void* x, void* x8, float* descale, int B, int H,
@@ -271,9 +285,11 @@ extern "C" int attn_prep_fp8_per_tensor(const void* x, void* x8, float* descale,
   if (rc != ATTN_OK || B == 0 || N == 0) return rc;
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  CUtensorMap mx;
+  if ((rc = map_prep(&mx, x, B, N, H, d)) != ATTN_OK) return rc;
   const int group = signs ? H / sign_heads : 1;
-  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
-                         nullptr, 1, static_cast<cudaStream_t>(stream));
+  return launch_prep_fp8(mx, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
+                         nullptr, 1, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_rope_table(float* rope_cos, float* rope_sin, int64_t N, int d, double base,
@@ -300,9 +316,11 @@ extern "C" int attn_prep_fp8_rope(const void* x, void* x8, float* descale, int B
   if (!aligned(rope_cos, 16) || !aligned(rope_sin, 16)) return ATTN_ERR_MISALIGNED;
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  CUtensorMap mx;
+  if ((rc = map_prep(&mx, x, B, N, H, d)) != ATTN_OK) return rc;
   const int group = signs ? H / sign_heads : 1;
-  return launch_prep_fp8(x, x8, descale, B, H, (int)N, d, signs, group, 0, rope_cos, rope_sin, 0,
-                         static_cast<cudaStream_t>(stream));
+  return launch_prep_fp8(mx, x8, descale, B, H, (int)N, d, signs, group, 0, rope_cos, rope_sin, 0,
+                         st->sm_count, st->status, static_cast<cudaStream_t>(stream));
 }
 
 namespace {

@@ -7,11 +7,14 @@
 // incoherent processing (each head multiplied by a random orthogonal matrix,
 // Hadamard x random signs, to spread outliers before quantisation).
 //
-// One CTA per (128-token block, head, batch); 8 warps x 16 rows; a half warp
-// holds one row (d/16 values per lane, loaded 16 bytes at a time, all rows of
-// the block in flight before any arithmetic).  The transform is a fast
-// Walsh-Hadamard butterfly (in-lane stages, then shuffles within the half
-// warp), scaled by 1/sqrt(d); the
+// A tile is one (128-token block, head, batch).  Persistent CTAs (two per SM
+// for d <= 128) walk the tiles with heads varying fastest; each CTA keeps a
+// ring of NS tiles in shared memory filled by TMA copies (one 128 x d box per
+// tile, rows past N zero-filled), so the next tiles stream in while the
+// current one is transformed and quantised.  8 warps x 16 rows; a half warp
+// holds one row (d/16 values per lane, read from shared memory 16 bytes at a
+// time).  The transform is a fast Walsh-Hadamard butterfly (in-lane stages,
+// then shuffles within the half warp), scaled by 1/sqrt(d); the
 // block amax is reduced through shared memory; codes are y * (448 / amax)
 // (float32, the reciprocal rounded once per block) rounded to nearest-even and
 // saturated to +-448 by the hardware conversion; descale = amax / 448.  The
@@ -28,6 +31,7 @@
 //   reduces the tensor's amax (atomic max of the float bits, all values >= 0),
 //   a second quantises every block with that amax, and a one-CTA kernel
 //   writes the descale of every block.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -37,19 +41,22 @@
 
 namespace attn {
 
-// 16 bytes of bf16 input per lane; a half warp holds one row
+// 16 bytes of bf16 input per lane from shared memory; a half warp holds one row
 template <int D>
-__device__ __forceinline__ void load_row_part(const uint16_t* src, float (&y)[D / 16]) {
+__device__ __forceinline__ void load_row_part(uint32_t saddr, float (&y)[D / 16]) {
   constexpr int VEC = D / 16;
   if constexpr (VEC == 4) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
-    y[0] = __uint_as_float(w.x << 16); y[1] = __uint_as_float(w.x & 0xFFFF0000u);
-    y[2] = __uint_as_float(w.y << 16); y[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    uint32_t w0, w1;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(saddr));
+    y[0] = __uint_as_float(w0 << 16); y[1] = __uint_as_float(w0 & 0xFFFF0000u);
+    y[2] = __uint_as_float(w1 << 16); y[3] = __uint_as_float(w1 & 0xFFFF0000u);
   } else {
 #pragma unroll
     for (int q = 0; q < VEC / 8; ++q) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + q);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      uint32_t ws[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(ws[0]), "=r"(ws[1]), "=r"(ws[2]), "=r"(ws[3])
+                   : "r"(saddr + 16 * q));
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         y[8 * q + 2 * i] = __uint_as_float(ws[i] << 16);
@@ -58,6 +65,36 @@ __device__ __forceinline__ void load_row_part(const uint16_t* src, float (&y)[D 
     }
   }
 }
+
+// ring depth and CTAs per SM of the prep kernel
+template <int D>
+struct PrepCfg {
+  static constexpr int TILE_BYTES = 128 * D * 2;   // one bf16 tile (128 rows x d)
+  static constexpr int NS = D == 64 ? 4 : 3;        // tiles in flight per CTA
+  static constexpr int CTAS_PER_SM = D == 256 ? 1 : 2;
+  static constexpr int TAIL = 256;                  // barriers, amax scratch, flags
+  static int smem_bytes(int transpose_out) {
+    return 128 + NS * TILE_BYTES + (transpose_out ? D * 128 : 0) + TAIL;
+  }
+};
+
+constexpr long long kPrepWaitCycles = 4000000000LL;   // about 2 s
+
+// arguments of one prep launch
+struct PrepLaunch {
+  const CUtensorMap* map;   // x as (d, H, N, B), box d x 1 x 128 x 1, no swizzle
+  uint8_t* x8;
+  float* descale;
+  const int8_t* signs;
+  int sign_group;
+  int B, H, N, nb, Npad;
+  const float* rope_cos;
+  const float* rope_sin;
+  float* tensor_amax;
+  int sm_count;
+  unsigned int* status;
+  cudaStream_t stream;
+};
 
 // quantisation modes
 enum PrepMode : int {
@@ -76,166 +113,224 @@ __device__ __forceinline__ void load_f32(const float* src, float (&t)[VEC]) {
 }
 
 template <int D, int MODE, bool ROPE>
-__global__ void __launch_bounds__(256) prep_fp8_kernel(const uint16_t* __restrict__ x,
-                                                       uint8_t* __restrict__ x8,
-                                                       float* __restrict__ descale,
-                                                       const int8_t* __restrict__ signs,
-                                                       int sign_group, int H, int N, int nb,
-                                                       int Npad, int transpose_out,
-                                                       const float* __restrict__ rope_cos,
-                                                       const float* __restrict__ rope_sin,
-                                                       float* tensor_amax) {
+__global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
+    prep_fp8_kernel(const __grid_constant__ CUtensorMap tmX, uint8_t* __restrict__ x8,
+                    float* __restrict__ descale, const int8_t* __restrict__ signs,
+                    int sign_group, int B, int H, int N, int nb, int Npad, int transpose_out,
+                    const float* __restrict__ rope_cos, const float* __restrict__ rope_sin,
+                    float* tensor_amax, unsigned int* status) {
+  using PC = PrepCfg<D>;
   constexpr int VEC = D / 16;  // elements per lane (a half warp covers one row)
   constexpr int ITERS = 8;     // 8 warps x 2 rows x 8 iterations = 128 rows
-  __shared__ float s_amax[8];
-  __shared__ __align__(16) uint8_t s_t[D * 128];  // transposed block (channel-major)
+  constexpr int NS = PC::NS;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sraw = ptx::smem_addr(smem_raw);
+  const uint32_t pad = (128u - (sraw & 127u)) & 127u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = sraw + pad;                           // NS tiles
+  uint8_t* s_t = smem + NS * PC::TILE_BYTES;                   // transposed codes
+  uint8_t* tail = s_t + (transpose_out ? D * 128 : 0);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tail);          // [NS] tile landed
+  float* s_amax = reinterpret_cast<float*>(tail + 8 * NS);     // [8]
+  auto bar = [&](int i) { return ptx::smem_addr(&bars[i]); };
 
-  // heads vary fastest across the grid, so that CTAs running together read
-  // neighbouring pieces of the same token rows ([B, N, H, d] layout)
-  const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
   const int e0 = hl * VEC;  // first channel of this lane
-  // row of iteration i: blk*128 + warp*16 + 2i + half
-  auto row_of = [&](int i) { return blk * 128 + warp * 16 + 2 * i + half; };
+  const long long n_tiles = (long long)B * nb * H;
+  const long long G = gridDim.x;
 
-  float sg[VEC];
-#pragma unroll
-  for (int v = 0; v < VEC; ++v)
-    sg[v] = signs ? (float)signs[(long long)(h / sign_group) * D + e0 + v] : 1.f;
-
-  float y[ITERS][VEC];
-  // issue every load of the block before any arithmetic on it
-#pragma unroll
-  for (int i = 0; i < ITERS; ++i) {
-    const int n = row_of(i);
-    if (n < N) {
-      load_row_part<D>(x + (((long long)b * N + n) * H + h) * D + e0, y[i]);
-    } else {
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) y[i][v] = 0.f;
-    }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) ptx::mbar_init(bar(i), 1);
+    ptx::fence_barrier_init();
+    ptx::tma_prefetch_desc(&tmX);
   }
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < ITERS; ++i) {
-    if constexpr (ROPE) {
-      // (y_c, y_{c+D/2}) -> (y_c cos - y_{c+D/2} sin, y_{c+D/2} cos + y_c sin);
-      // lane hl holds channels hl*VEC.., its partner lane hl ^ 8
-      const int n = row_of(i);
-      float cs[VEC], sn[VEC];
-      if (n < N) {
-        const long long off = (long long)n * (D / 2) + (hl & 7) * VEC;
-        load_f32<VEC>(rope_cos + off, cs);
-        load_f32<VEC>(rope_sin + off, sn);
-      } else {
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) { cs[v] = 1.f; sn[v] = 0.f; }
-      }
-      const bool upper = hl >= 8;
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) {
-        const float other = __shfl_xor_sync(0xffffffffu, y[i][v], 8);
-        const float t = upper ? other * sn[v] : -(other * sn[v]);
-        y[i][v] = fmaf(y[i][v], cs[v], t);
-      }
+  __syncthreads();
+  // tile t: heads fastest, then blocks, then batch
+  auto issue = [&](long long k) {   // copy the CTA's k-th tile into stage k % NS
+    const long long t = blockIdx.x + k * G;
+    if (t >= n_tiles) return;
+    const int th = (int)(t % H);
+    const long long r = t / H;
+    const int tblk = (int)(r % nb), tb = (int)(r / nb);
+    const int st = (int)(k % NS);
+    ptx::mbar_arrive_expect_tx(bar(st), PC::TILE_BYTES);
+    ptx::tma_load_4d(sbase + st * PC::TILE_BYTES, &tmX, bar(st), 0, th, tblk * 128, tb);
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < NS; ++k) issue(k);
+
+  for (long long k = 0;; ++k) {
+    const long long t = blockIdx.x + k * G;
+    if (t >= n_tiles) break;
+    const int h = (int)(t % H);
+    const long long rr = t / H;
+    const int blk = (int)(rr % nb), b = (int)(rr / nb);
+    const int st = (int)(k % NS);
+    // bounded wait for the tile; every thread takes the same decision
+    bool ok = ptx::mbar_try_wait(bar(st), (uint32_t)((k / NS) & 1));
+    if (!ok) {
+      const long long t0 = clock64();
+      while (!(ok = ptx::mbar_try_wait_sleep(bar(st), (uint32_t)((k / NS) & 1), 100000)))
+        if (clock64() - t0 > kPrepWaitCycles) break;
     }
-    if (signs) {
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        atomicOr(status, 1u);
+        // wait (bounded) for the copies this CTA still has in flight
+        for (long long kk = k; kk < k + NS; ++kk) {
+          if (blockIdx.x + kk * G >= n_tiles) break;
+          const long long t0 = clock64();
+          while (!ptx::mbar_try_wait(bar((int)(kk % NS)), (uint32_t)((kk / NS) & 1)))
+            if (clock64() - t0 > kPrepWaitCycles) break;
+        }
+      }
+      return;
+    }
+    // row of iteration i within the tile: warp*16 + 2i + half
+    auto row_of = [&](int i) { return blk * 128 + warp * 16 + 2 * i + half; };
+    const uint32_t tile = sbase + st * PC::TILE_BYTES;
+
+    float sg[VEC];
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) y[i][v] *= sg[v];
-      // butterfly stages inside the lane (channel bit < log2 VEC)
+    for (int v = 0; v < VEC; ++v)
+      sg[v] = signs ? (float)signs[(long long)(h / sign_group) * D + e0 + v] : 1.f;
+
+    float y[ITERS][VEC];
+    // the whole tile from shared memory (rows past N were zero-filled by the copy)
 #pragma unroll
-      for (int hs = 1; hs < VEC; hs <<= 1) {
+    for (int i = 0; i < ITERS; ++i)
+      load_row_part<D>(tile + (uint32_t)((warp * 16 + 2 * i + half) * D + e0) * 2, y[i]);
+    __syncthreads();   // stage st is free: refill it with the tile NS ahead
+    if (threadIdx.x == 0) issue(k + NS);
+
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < ITERS; ++i) {
+      if constexpr (ROPE) {
+        // (y_c, y_{c+D/2}) -> (y_c cos - y_{c+D/2} sin, y_{c+D/2} cos + y_c sin);
+        // lane hl holds channels hl*VEC.., its partner lane hl ^ 8
+        const int n = row_of(i);
+        float cs[VEC], sn[VEC];
+        if (n < N) {
+          const long long off = (long long)n * (D / 2) + (hl & 7) * VEC;
+          load_f32<VEC>(rope_cos + off, cs);
+          load_f32<VEC>(rope_sin + off, sn);
+        } else {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) { cs[v] = 1.f; sn[v] = 0.f; }
+        }
+        const bool upper = hl >= 8;
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-          if ((v & hs) == 0) {
-            const float a = y[i][v], c = y[i][v + hs];
-            y[i][v] = a + c;
-            y[i][v + hs] = a - c;
+          const float other = __shfl_xor_sync(0xffffffffu, y[i][v], 8);
+          const float t = upper ? other * sn[v] : -(other * sn[v]);
+          y[i][v] = fmaf(y[i][v], cs[v], t);
+        }
+      }
+      if (signs) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) y[i][v] *= sg[v];
+        // butterfly stages inside the lane (channel bit < log2 VEC)
+#pragma unroll
+        for (int hs = 1; hs < VEC; hs <<= 1) {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            if ((v & hs) == 0) {
+              const float a = y[i][v], c = y[i][v + hs];
+              y[i][v] = a + c;
+              y[i][v + hs] = a - c;
+            }
           }
         }
-      }
-      // butterfly stages across the 16 lanes of the half warp
+        // butterfly stages across the 16 lanes of the half warp: the lower
+        // lane keeps y + other, the upper one other - y (one FMA with +-1)
 #pragma unroll
-      for (int lm = 1; lm < 16; lm <<= 1) {
-        const bool upper = (hl & lm) != 0;
+        for (int lm = 1; lm < 16; lm <<= 1) {
+          const float sgn = (hl & lm) ? -1.f : 1.f;
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            const float other = __shfl_xor_sync(0xffffffffu, y[i][v], lm);
+            y[i][v] = fmaf(y[i][v], sgn, other);
+          }
+        }
+        // the 1 / sqrt(d) of the transform is applied with the quantisation scale
+      }
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) amax = fmaxf(amax, fabsf(y[i][v]));
+    }
+
+    float bmax;
+    // with the transform, y is still missing its factor 1 / sqrt(d): amax is
+    // that of the scaled values, y is scaled together with the quantisation
+    const float inv_sqrt_d =
+        !signs ? 1.f : (D == 64) ? 0.125f : (D == 128) ? 0.08838834764831845f : 0.0625f;
+    if constexpr (MODE == kPrepTensor) {
+      bmax = *tensor_amax;   // written by the amax pass, read-only here
+    } else {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0) s_amax[warp] = amax;
+      __syncthreads();
+      bmax = s_amax[0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, s_amax[w]);
+      if (signs) bmax *= inv_sqrt_d;
+    }
+    if constexpr (MODE == kPrepTensorAmax) {
+      // non-negative floats order like their bit patterns
+      if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(tensor_amax), __float_as_uint(bmax));
+      continue;
+    }
+    // codes are y * (448 / amax), the reciprocal taken once per block
+    // (times 1 / sqrt(d) with the transform)
+    float inv_ds = bmax > 0.f ? __fdiv_rn(448.0f, bmax) : 1.0f;
+    if (signs) inv_ds *= inv_sqrt_d;
+    if constexpr (MODE == kPrepBlock) {
+      const float ds = bmax > 0.f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
+      if (threadIdx.x == 0) descale[((long long)b * H + h) * nb + blk] = ds;
+    }
+
+#pragma unroll
+    for (int i = 0; i < ITERS; ++i) {
+      const int n = row_of(i);
+      const int nl = n - blk * 128;
+      uint32_t c4[VEC / 4];
+#pragma unroll
+      for (int q = 0; q < VEC / 4; ++q)
+        c4[q] = ptx::pack_e4m3x4(y[i][4 * q] * inv_ds, y[i][4 * q + 1] * inv_ds,
+                                 y[i][4 * q + 2] * inv_ds, y[i][4 * q + 3] * inv_ds);
+      if (!transpose_out) {
+        if (n < N) {
+          uint8_t* dst = x8 + (((long long)b * N + n) * H + h) * D + e0;
+          if constexpr (VEC == 4) {
+            *reinterpret_cast<uint32_t*>(dst) = c4[0];
+          } else if constexpr (VEC == 8) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(c4[0], c4[1]);
+          } else {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+          }
+        }
+      } else {
+        // stage codes channel-major: s_t[e][nl ^ swz(e)] (rows n >= N hold zeros);
+        // the XOR swizzle puts the 16 channels a half warp writes in distinct banks
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-          const float other = __shfl_xor_sync(0xffffffffu, y[i][v], lm);
-          y[i][v] = upper ? (other - y[i][v]) : (y[i][v] + other);
+          const int e = e0 + v;
+          s_t[e * 128 + (nl ^ (((e / VEC) & 31) << 2))] = (uint8_t)((c4[v >> 2] >> (8 * (v & 3))) & 0xFF);
         }
       }
-      const float inv_sqrt_d = (D == 64) ? 0.125f : (D == 128) ? 0.08838834764831845f : 0.0625f;
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) y[i][v] *= inv_sqrt_d;
     }
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) amax = fmaxf(amax, fabsf(y[i][v]));
-  }
-
-  float bmax;
-  if constexpr (MODE == kPrepTensor) {
-    bmax = *tensor_amax;   // written by the amax pass, read-only here
-  } else {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) s_amax[warp] = amax;
-    __syncthreads();
-    bmax = s_amax[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, s_amax[w]);
-  }
-  if constexpr (MODE == kPrepTensorAmax) {
-    // non-negative floats order like their bit patterns
-    if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(tensor_amax), __float_as_uint(bmax));
-    return;
-  }
-  // codes are y * (448 / amax), the reciprocal taken once per block
-  const float inv_ds = bmax > 0.f ? __fdiv_rn(448.0f, bmax) : 1.0f;
-  if constexpr (MODE == kPrepBlock) {
-    const float ds = bmax > 0.f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
-    if (threadIdx.x == 0) descale[((long long)b * H + h) * nb + blk] = ds;
-  }
-
-#pragma unroll
-  for (int i = 0; i < ITERS; ++i) {
-    const int n = row_of(i);
-    const int nl = n - blk * 128;
-    uint32_t c4[VEC / 4];
-#pragma unroll
-    for (int q = 0; q < VEC / 4; ++q)
-      c4[q] = ptx::pack_e4m3x4(y[i][4 * q] * inv_ds, y[i][4 * q + 1] * inv_ds,
-                               y[i][4 * q + 2] * inv_ds, y[i][4 * q + 3] * inv_ds);
-    if (!transpose_out) {
-      if (n < N) {
-        uint8_t* dst = x8 + (((long long)b * N + n) * H + h) * D + e0;
-        if constexpr (VEC == 4) {
-          *reinterpret_cast<uint32_t*>(dst) = c4[0];
-        } else if constexpr (VEC == 8) {
-          *reinterpret_cast<uint2*>(dst) = make_uint2(c4[0], c4[1]);
-        } else {
-          *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+    if (transpose_out) {
+      __syncthreads();
+      // row e of the transposed block: 128 keys = 32 lanes x 4 bytes
+      const int valid = min(128, Npad - blk * 128);  // multiple of 16
+      for (int e = warp; e < D; e += 8) {
+        if (lane * 4 < valid) {
+          uint8_t* dst = x8 + (((long long)b * H + h) * D + e) * Npad + blk * 128 + lane * 4;
+          *reinterpret_cast<uint32_t*>(dst) =
+              *reinterpret_cast<const uint32_t*>(&s_t[e * 128 + ((lane * 4) ^ (((e / VEC) & 31) << 2))]);
         }
-      }
-    } else {
-      // stage codes channel-major: s_t[e][nl ^ swz(e)] (rows n >= N hold zeros);
-      // the XOR swizzle puts the 16 channels a half warp writes in distinct banks
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) {
-        const int e = e0 + v;
-        s_t[e * 128 + (nl ^ (((e / VEC) & 31) << 2))] = (uint8_t)((c4[v >> 2] >> (8 * (v & 3))) & 0xFF);
-      }
-    }
-  }
-  if (transpose_out) {
-    __syncthreads();
-    // row e of the transposed block: 128 keys = 32 lanes x 4 bytes
-    const int valid = min(128, Npad - blk * 128);  // multiple of 16
-    for (int e = warp; e < D; e += 8) {
-      if (lane * 4 < valid) {
-        uint8_t* dst = x8 + (((long long)b * H + h) * D + e) * Npad + blk * 128 + lane * 4;
-        *reinterpret_cast<uint32_t*>(dst) =
-            *reinterpret_cast<const uint32_t*>(&s_t[e * 128 + ((lane * 4) ^ (((e / VEC) & 31) << 2))]);
       }
     }
   }
@@ -272,67 +367,65 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cos
 }
 
 template <int D, int MODE, bool ROPE>
-void launch_prep_instance(dim3 grid, cudaStream_t stream, const uint16_t* xs, uint8_t* xo,
-                          float* descale, const int8_t* signs, int sign_group, int H, int N,
-                          int nb, int Npad, int transpose_out, const float* rc, const float* rs,
-                          float* tamax) {
-  prep_fp8_kernel<D, MODE, ROPE><<<grid, 256, 0, stream>>>(
-      xs, xo, descale, signs, sign_group, H, N, nb, Npad, transpose_out, rc, rs, tamax);
-}
-
-template <int MODE, bool ROPE>
-int launch_prep_d(int d, dim3 grid, cudaStream_t stream, const uint16_t* xs, uint8_t* xo,
-                  float* descale, const int8_t* signs, int sign_group, int H, int N, int nb,
-                  int Npad, int transpose_out, const float* rc, const float* rs, float* tamax) {
-  switch (d) {
-    case 64:
-      launch_prep_instance<64, MODE, ROPE>(grid, stream, xs, xo, descale, signs, sign_group, H,
-                                           N, nb, Npad, transpose_out, rc, rs, tamax);
-      break;
-    case 128:
-      launch_prep_instance<128, MODE, ROPE>(grid, stream, xs, xo, descale, signs, sign_group, H,
-                                            N, nb, Npad, transpose_out, rc, rs, tamax);
-      break;
-    case 256:
-      launch_prep_instance<256, MODE, ROPE>(grid, stream, xs, xo, descale, signs, sign_group, H,
-                                            N, nb, Npad, transpose_out, rc, rs, tamax);
-      break;
-    default:
-      return ATTN_ERR_UNSUPPORTED;
-  }
+int launch_prep_instance(const PrepLaunch& L, int mode_transpose) {
+  auto kern = prep_fp8_kernel<D, MODE, ROPE>;
+  const int smem = PrepCfg<D>::smem_bytes(mode_transpose);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prep)");
+  const long long tiles = (long long)L.B * L.nb * L.H;
+  const long long cap = (long long)PrepCfg<D>::CTAS_PER_SM * L.sm_count;
+  const int grid = (int)(tiles < cap ? tiles : cap);
+  kern<<<grid, 256, smem, L.stream>>>(*L.map, L.x8, L.descale, L.signs, L.sign_group, L.B, L.H,
+                                      L.N, L.nb, L.Npad, mode_transpose, L.rope_cos, L.rope_sin,
+                                      L.tensor_amax, L.status);
   note_launch();
   return check_launch();
 }
 
-int launch_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int N, int d,
+template <int MODE, bool ROPE>
+int launch_prep_d(int d, const PrepLaunch& L, int transpose_out) {
+  switch (d) {
+    case 64: return launch_prep_instance<64, MODE, ROPE>(L, transpose_out);
+    case 128: return launch_prep_instance<128, MODE, ROPE>(L, transpose_out);
+    case 256: return launch_prep_instance<256, MODE, ROPE>(L, transpose_out);
+    default: return ATTN_ERR_UNSUPPORTED;
+  }
+}
+
+int launch_prep_fp8(const CUtensorMap& map_x, void* x8, float* descale, int B, int H, int N, int d,
                     const int8_t* signs, int sign_group, int transpose_out, const float* rope_cos,
-                    const float* rope_sin, int per_tensor, cudaStream_t stream) {
-  const int nb = (N + 127) / 128;
-  const int Npad = (N + 15) / 16 * 16;
-  dim3 grid(H, nb, B);
-  const uint16_t* xs = static_cast<const uint16_t*>(x);
-  uint8_t* xo = static_cast<uint8_t*>(x8);
+                    const float* rope_sin, int per_tensor, int sm_count, unsigned int* status,
+                    cudaStream_t stream) {
+  PrepLaunch L{};
+  L.map = &map_x;
+  L.x8 = static_cast<uint8_t*>(x8);
+  L.descale = descale;
+  L.signs = signs;
+  L.sign_group = sign_group;
+  L.B = B;
+  L.H = H;
+  L.N = N;
+  L.nb = (N + 127) / 128;
+  L.Npad = (N + 15) / 16 * 16;
+  L.rope_cos = rope_cos;
+  L.rope_sin = rope_sin;
+  L.sm_count = sm_count;
+  L.status = status;
+  L.stream = stream;
   if (!per_tensor) {
-    if (rope_cos)
-      return launch_prep_d<kPrepBlock, true>(d, grid, stream, xs, xo, descale, signs, sign_group,
-                                             H, N, nb, Npad, transpose_out, rope_cos, rope_sin,
-                                             nullptr);
-    return launch_prep_d<kPrepBlock, false>(d, grid, stream, xs, xo, descale, signs, sign_group,
-                                            H, N, nb, Npad, transpose_out, nullptr, nullptr,
-                                            nullptr);
+    if (rope_cos) return launch_prep_d<kPrepBlock, true>(d, L, transpose_out);
+    return launch_prep_d<kPrepBlock, false>(d, L, transpose_out);
   }
   if (rope_cos) return ATTN_ERR_UNSUPPORTED;
   // the tensor amax is accumulated in descale[0] and read from there
   cudaError_t e = cudaMemsetAsync(descale, 0, sizeof(float), stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(descale)");
-  int rc = launch_prep_d<kPrepTensorAmax, false>(d, grid, stream, xs, xo, descale, signs,
-                                                 sign_group, H, N, nb, Npad, transpose_out,
-                                                 nullptr, nullptr, descale);
+  L.tensor_amax = descale;
+  int rc = launch_prep_d<kPrepTensorAmax, false>(d, L, 0);
   if (rc != ATTN_OK) return rc;
-  rc = launch_prep_d<kPrepTensor, false>(d, grid, stream, xs, xo, descale, signs, sign_group, H,
-                                         N, nb, Npad, transpose_out, nullptr, nullptr, descale);
+  rc = launch_prep_d<kPrepTensor, false>(d, L, transpose_out);
   if (rc != ATTN_OK) return rc;
-  prep_fill_descale_kernel<<<1, 256, 0, stream>>>(descale, (long long)B * H * nb);
+  prep_fill_descale_kernel<<<1, 256, 0, stream>>>(descale, (long long)B * H * L.nb);
   note_launch();
   return check_launch();
 }

@@ -40,9 +40,12 @@ int launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, fl
 // per_tensor: one scale for the tensor (descale[0] is used as the amax
 // accumulator, then every block's descale is written); rope_cos / rope_sin:
 // NULL or float32 [N, d/2] tables, rotation before the transform
-int launch_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int N, int d,
+// map_x: x [B, N, H, d] bf16 as TMA dims (d, H, N, B), box d x 1 x 128 x 1,
+// no swizzle (encode_prep_map)
+int launch_prep_fp8(const CUtensorMap& map_x, void* x8, float* descale, int B, int H, int N, int d,
                     const int8_t* signs, int sign_group, int transpose_out, const float* rope_cos,
-                    const float* rope_sin, int per_tensor, cudaStream_t stream);
+                    const float* rope_sin, int per_tensor, int sm_count, unsigned int* status,
+                    cudaStream_t stream);
 int launch_rope_table(float* cos_out, float* sin_out, int N, int d, double base, long long pos0,
                       cudaStream_t stream);
 
