@@ -59,13 +59,21 @@ def attention_flops(B, Hq, Nq, Nk, d, causal):
     return f / 2 if causal else f
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: ncu counters taken on other sources are stale."""
+# CUDA sources each timed kernel is built from (its launch set-up included)
+FWD_SOURCES = ("attn_fwd_kernel.cuh", "fwd_launch.cuh", "ptx.cuh", "internal.h", "api.cu",
+               "attn_fwd_f16.cu", "attn_fwd_bf16.cu", "attn_fwd_e4m3.cu")
+MERGE_SOURCES = FWD_SOURCES + ("splitkv_merge.cu",)
+
+
+def kernel_source_hash(names=FWD_SOURCES) -> str:
+    """Hash of the CUDA sources of a kernel: ncu counters taken on other
+    sources are stale."""
     csrc = os.path.join(ROOT, "tiled_attention_forward_02_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
+    for name in sorted(names):
+        path = os.path.join(csrc, name)
+        if os.path.exists(path):
+            with open(path, "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
@@ -87,7 +95,8 @@ def recorded_traffic(kernel: str, workload: str):
     with open(path) as f:
         rec = json.load(f)
     e = rec.get(f"{kernel}|{workload}")
-    if not e or e.get("source_hash") != kernel_source_hash():
+    names = MERGE_SOURCES if "merge" in kernel else FWD_SOURCES
+    if not e or e.get("source_hash") != kernel_source_hash(names):
         return None
     return e.get("dram_bytes_per_launch")
 
