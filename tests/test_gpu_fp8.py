@@ -282,3 +282,32 @@ def test_fp8_forward_variants_vs_dequantised_oracle(gpu_lib, variant):
     assert e["o_rel_rms"] <= 4e-2, e
     exact_codes = variant == "per_tensor"
     assert e["lse_max_abs"] <= (2e-3 if exact_codes else 1e-2), e
+
+
+def test_prep_rope_hadamard_full_size_sampled(gpu_lib):
+    """The rotary + transform prep at the FP8 workload's size (B=4, H=16,
+    N=4096, d=128, x50 outliers), in the launch configuration the bench uses:
+    every descale, and the codes of sampled rows, against the oracle."""
+    B, N, H, d = 4, 4096, 16, 128
+    q, _, _ = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=0,
+                                outlier_frac=1e-3, device="cuda")
+    cos, sin = gpu_lib.attn_rope_table(N, d)
+    signs = _signs(H, d)
+    codes, ds = gpu_lib.attn_prep_fp8_rope(q, cos, sin, signs=signs, sign_heads=H)
+    assert gpu_lib.get_status() == 0
+    x = q.double().cpu().numpy()
+    _, ods, _ = ofp8.prepare(x, signs.cpu().numpy(), True, rope_base=10000.0)
+    g_ds = ds.cpu().numpy()
+    np.testing.assert_allclose(g_ds, ods, rtol=4e-6, atol=0)
+    rows = synth.sample_rows(B, H, N, per_head=16, seed=3)
+    # exact rotated + transformed values of the sampled rows only
+    xr = x[rows[:, 0], rows[:, 2], rows[:, 1]]                       # [R, d]
+    cos_t, sin_t = ofp8.rope_tables(N, d, 10000.0)
+    c, s_ = cos_t[rows[:, 2]], sin_t[rows[:, 2]]
+    a, b = xr[:, : d // 2], xr[:, d // 2:]
+    rot = np.concatenate([a * c - b * s_, b * c + a * s_], axis=-1)
+    sg = signs.cpu().numpy().astype(np.float64)[rows[:, 1]]
+    y = (rot * sg) @ ofp8.hadamard_matrix(d).astype(np.float64) / np.sqrt(d)
+    q_exact = y / g_ds.astype(np.float64)[rows[:, 0], rows[:, 1], rows[:, 2] // 128][:, None]
+    g = codes.cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
+    _codes_near(g, q_exact)

@@ -11,10 +11,13 @@
 // for d <= 128) walk the tiles with heads varying fastest; each CTA keeps a
 // ring of NS tiles in shared memory filled by TMA copies (one 128 x d box per
 // tile, rows past N zero-filled), so the next tiles stream in while the
-// current one is transformed and quantised.  8 warps x 16 rows; a half warp
-// holds one row (d/16 values per lane, read from shared memory 16 bytes at a
-// time).  The transform is a fast Walsh-Hadamard butterfly (in-lane stages,
-// then shuffles within the half warp), scaled by 1/sqrt(d); the
+// current one is transformed and quantised.  8 warps x 16 rows; LPR lanes
+// hold one row (8 for d <= 128, 16 for d = 256), lane l owning the 16-byte
+// chunks l, l + LPR, ... of 8 channels each, so that 8 lanes read 128
+// contiguous bytes of shared memory (no bank conflicts) and the rotary pair
+// (c, c + d/2) lies in one lane for d >= 128.  The transform is a fast
+// Walsh-Hadamard butterfly (stages over the in-lane channel bits, then
+// shuffles across the LPR lanes of the row), scaled by 1/sqrt(d); the
 // block amax is reduced through shared memory; codes are y * (448 / amax)
 // (float32, the reciprocal rounded once per block) rounded to nearest-even and
 // saturated to +-448 by the hardware conversion; descale = amax / 448.  The
@@ -24,9 +27,9 @@
 // Two variants share the kernel:
 // * rotary embedding before the transform (the summary card notes that the
 //   transform can ride along with the rotary embedding, a bandwidth-bound
-//   step): rotate-half form, channel c paired with c + d/2; the pair sits in
-//   lanes hl and hl ^ 8 of the half warp, one shuffle per value; cos and sin
-//   come from float32 tables [N, d/2] (attn_rope_table);
+//   step): rotate-half form, channel c paired with c + d/2 (in the same lane
+//   for d >= 128, one shuffle per value for d = 64); cos and sin come from
+//   float32 tables [N, d/2] (attn_rope_table);
 // * one scale per tensor (the baseline FP8 scheme): a first pass only
 //   reduces the tensor's amax (atomic max of the float bits, all values >= 0),
 //   a second quantises every block with that amax, and a one-CTA kernel
@@ -41,28 +44,16 @@
 
 namespace attn {
 
-// 16 bytes of bf16 input per lane from shared memory; a half warp holds one row
-template <int D>
-__device__ __forceinline__ void load_row_part(uint32_t saddr, float (&y)[D / 16]) {
-  constexpr int VEC = D / 16;
-  if constexpr (VEC == 4) {
-    uint32_t w0, w1;
-    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(saddr));
-    y[0] = __uint_as_float(w0 << 16); y[1] = __uint_as_float(w0 & 0xFFFF0000u);
-    y[2] = __uint_as_float(w1 << 16); y[3] = __uint_as_float(w1 & 0xFFFF0000u);
-  } else {
+// one 16-byte chunk (8 bf16 channels) from shared memory, widened to float
+__device__ __forceinline__ void load_chunk(uint32_t saddr, float* y) {
+  uint32_t ws[4];
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(ws[0]), "=r"(ws[1]), "=r"(ws[2]), "=r"(ws[3])
+               : "r"(saddr));
 #pragma unroll
-    for (int q = 0; q < VEC / 8; ++q) {
-      uint32_t ws[4];
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(ws[0]), "=r"(ws[1]), "=r"(ws[2]), "=r"(ws[3])
-                   : "r"(saddr + 16 * q));
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        y[8 * q + 2 * i] = __uint_as_float(ws[i] << 16);
-        y[8 * q + 2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
-      }
-    }
+  for (int i = 0; i < 4; ++i) {
+    y[2 * i] = __uint_as_float(ws[i] << 16);
+    y[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
   }
 }
 
@@ -70,6 +61,8 @@ __device__ __forceinline__ void load_row_part(uint32_t saddr, float (&y)[D / 16]
 template <int D>
 struct PrepCfg {
   static constexpr int TILE_BYTES = 128 * D * 2;   // one bf16 tile (128 rows x d)
+  static constexpr int LPR = D == 256 ? 16 : 8;     // lanes per row
+  static constexpr int CH = D / (8 * LPR);          // 16-byte chunks (8 channels) per lane
   static constexpr int NS = D == 64 ? 4 : 3;        // tiles in flight per CTA
   static constexpr int CTAS_PER_SM = D == 256 ? 1 : 2;
   static constexpr int TAIL = 256;                  // barriers, amax scratch, flags
@@ -120,8 +113,11 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
                     const float* __restrict__ rope_cos, const float* __restrict__ rope_sin,
                     float* tensor_amax, unsigned int* status) {
   using PC = PrepCfg<D>;
-  constexpr int VEC = D / 16;  // elements per lane (a half warp covers one row)
-  constexpr int ITERS = 8;     // 8 warps x 2 rows x 8 iterations = 128 rows
+  constexpr int LPR = PC::LPR;        // lanes per row
+  constexpr int CH = PC::CH;          // chunks of 8 channels per lane
+  constexpr int VEC = 8 * CH;         // channels per lane
+  constexpr int RPW = 32 / LPR;       // rows per warp and iteration
+  constexpr int ITERS = 16 / RPW;     // 8 warps x 16 rows = 128 rows
   constexpr int NS = PC::NS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = ptx::smem_addr(smem_raw);
@@ -135,8 +131,9 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   auto bar = [&](int i) { return ptx::smem_addr(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = lane >> 4, hl = lane & 15;
-  const int e0 = hl * VEC;  // first channel of this lane
+  const int rsub = lane / LPR, hl = lane % LPR;
+  // channel of value v = 8 j + t of this lane: 8 (hl + LPR j) + t
+  auto chan = [&](int v) { return 8 * (hl + LPR * (v >> 3)) + (v & 7); };
   const long long n_tiles = (long long)B * nb * H;
   const long long G = gridDim.x;
 
@@ -187,20 +184,23 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
       }
       return;
     }
-    // row of iteration i within the tile: warp*16 + 2i + half
-    auto row_of = [&](int i) { return blk * 128 + warp * 16 + 2 * i + half; };
+    // row of iteration i within the tile: warp*16 + RPW*i + rsub
+    auto row_of = [&](int i) { return blk * 128 + warp * 16 + RPW * i + rsub; };
     const uint32_t tile = sbase + st * PC::TILE_BYTES;
 
     float sg[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v)
-      sg[v] = signs ? (float)signs[(long long)(h / sign_group) * D + e0 + v] : 1.f;
+      sg[v] = signs ? (float)signs[(long long)(h / sign_group) * D + chan(v)] : 1.f;
 
     float y[ITERS][VEC];
     // the whole tile from shared memory (rows past N were zero-filled by the copy)
 #pragma unroll
     for (int i = 0; i < ITERS; ++i)
-      load_row_part<D>(tile + (uint32_t)((warp * 16 + 2 * i + half) * D + e0) * 2, y[i]);
+#pragma unroll
+      for (int j = 0; j < CH; ++j)
+        load_chunk(tile + (uint32_t)((warp * 16 + RPW * i + rsub) * D * 2 + (hl + LPR * j) * 16),
+                   &y[i][8 * j]);
     __syncthreads();   // stage st is free: refill it with the tile NS ahead
     if (threadIdx.x == 0) issue(k + NS);
 
@@ -208,30 +208,49 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
 #pragma unroll
     for (int i = 0; i < ITERS; ++i) {
       if constexpr (ROPE) {
-        // (y_c, y_{c+D/2}) -> (y_c cos - y_{c+D/2} sin, y_{c+D/2} cos + y_c sin);
-        // lane hl holds channels hl*VEC.., its partner lane hl ^ 8
+        // (y_c, y_{c+D/2}) -> (y_c cos - y_{c+D/2} sin, y_{c+D/2} cos + y_c sin).
+        // With two or more chunks per lane the partner of chunk j is chunk
+        // j ^ CH/2 of the same lane; with one (d = 64) it is lane hl ^ LPR/2.
         const int n = row_of(i);
         float cs[VEC], sn[VEC];
         if (n < N) {
-          const long long off = (long long)n * (D / 2) + (hl & 7) * VEC;
-          load_f32<VEC>(rope_cos + off, cs);
-          load_f32<VEC>(rope_sin + off, sn);
+#pragma unroll
+          for (int v = 0; v < VEC; v += 4) {
+            const int c = chan(v) % (D / 2);
+            const float4 c4 = __ldg(reinterpret_cast<const float4*>(rope_cos + (long long)n * (D / 2) + c));
+            const float4 s4 = __ldg(reinterpret_cast<const float4*>(rope_sin + (long long)n * (D / 2) + c));
+            cs[v] = c4.x; cs[v + 1] = c4.y; cs[v + 2] = c4.z; cs[v + 3] = c4.w;
+            sn[v] = s4.x; sn[v + 1] = s4.y; sn[v + 2] = s4.z; sn[v + 3] = s4.w;
+          }
         } else {
 #pragma unroll
           for (int v = 0; v < VEC; ++v) { cs[v] = 1.f; sn[v] = 0.f; }
         }
-        const bool upper = hl >= 8;
+        if constexpr (CH >= 2) {
+          float r[VEC];
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-          const float other = __shfl_xor_sync(0xffffffffu, y[i][v], 8);
-          const float t = upper ? other * sn[v] : -(other * sn[v]);
-          y[i][v] = fmaf(y[i][v], cs[v], t);
+          for (int v = 0; v < VEC; ++v) {
+            const int pv = v ^ (4 * CH);   // chunk j ^ CH/2, same offset in the chunk
+            const bool upper = (v & (4 * CH)) != 0;
+            r[v] = fmaf(y[i][v], cs[v], upper ? y[i][pv] * sn[v] : -(y[i][pv] * sn[v]));
+          }
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) y[i][v] = r[v];
+        } else {
+          const bool upper = (hl & (LPR / 2)) != 0;
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            const float other = __shfl_xor_sync(0xffffffffu, y[i][v], LPR / 2);
+            const float t = upper ? other * sn[v] : -(other * sn[v]);
+            y[i][v] = fmaf(y[i][v], cs[v], t);
+          }
         }
       }
       if (signs) {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) y[i][v] *= sg[v];
-        // butterfly stages inside the lane (channel bit < log2 VEC)
+        // butterfly stages over the in-lane bits of the channel (the 3 bits
+        // within a chunk and the chunk-index bits above the lane bits)
 #pragma unroll
         for (int hs = 1; hs < VEC; hs <<= 1) {
 #pragma unroll
@@ -243,10 +262,10 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
             }
           }
         }
-        // butterfly stages across the 16 lanes of the half warp: the lower
-        // lane keeps y + other, the upper one other - y (one FMA with +-1)
+        // butterfly stages across the LPR lanes of the row: the lower lane
+        // keeps y + other, the upper one other - y (one FMA with +-1)
 #pragma unroll
-        for (int lm = 1; lm < 16; lm <<= 1) {
+        for (int lm = 1; lm < LPR; lm <<= 1) {
           const float sgn = (hl & lm) ? -1.f : 1.f;
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
@@ -302,22 +321,20 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
                                  y[i][4 * q + 2] * inv_ds, y[i][4 * q + 3] * inv_ds);
       if (!transpose_out) {
         if (n < N) {
-          uint8_t* dst = x8 + (((long long)b * N + n) * H + h) * D + e0;
-          if constexpr (VEC == 4) {
-            *reinterpret_cast<uint32_t*>(dst) = c4[0];
-          } else if constexpr (VEC == 8) {
-            *reinterpret_cast<uint2*>(dst) = make_uint2(c4[0], c4[1]);
-          } else {
-            *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
-          }
+          // chunk j of the lane: 8 codes at channel 8 (hl + LPR j)
+          uint8_t* dst = x8 + (((long long)b * N + n) * H + h) * D;
+#pragma unroll
+          for (int j = 0; j < CH; ++j)
+            *reinterpret_cast<uint2*>(dst + 8 * (hl + LPR * j)) = make_uint2(c4[2 * j], c4[2 * j + 1]);
         }
       } else {
-        // stage codes channel-major: s_t[e][nl ^ swz(e)] (rows n >= N hold zeros);
-        // the XOR swizzle puts the 16 channels a half warp writes in distinct banks
+        // stage codes channel-major: s_t[e][nl ^ swz(e)] (rows n >= N hold
+        // zeros); swz(e) = (chunk of e) x 4 puts the chunks written by one
+        // store in distinct banks (rows of a warp share a 4-byte word)
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-          const int e = e0 + v;
-          s_t[e * 128 + (nl ^ (((e / VEC) & 31) << 2))] = (uint8_t)((c4[v >> 2] >> (8 * (v & 3))) & 0xFF);
+          const int e = chan(v);
+          s_t[e * 128 + (nl ^ (((e >> 3) & 31) << 2))] = (uint8_t)((c4[v >> 2] >> (8 * (v & 3))) & 0xFF);
         }
       }
     }
@@ -329,7 +346,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
         if (lane * 4 < valid) {
           uint8_t* dst = x8 + (((long long)b * H + h) * D + e) * Npad + blk * 128 + lane * 4;
           *reinterpret_cast<uint32_t*>(dst) =
-              *reinterpret_cast<const uint32_t*>(&s_t[e * 128 + ((lane * 4) ^ (((e / VEC) & 31) << 2))]);
+              *reinterpret_cast<const uint32_t*>(&s_t[e * 128 + ((lane * 4) ^ (((e >> 3) & 31) << 2))]);
         }
       }
     }
