@@ -305,7 +305,11 @@ def config_of(wl):
 
 # ------------------------------------------------------------------ GPU arm
 def make_step(wl, dev):
-    """Return (step_fn, e2e_step_fn, meta) for the workload; inputs resident."""
+    """Return (step_fn, hot_fn, meta) for the workload; inputs resident.
+
+    hot_fn(q, k, v, o, lse) runs the whole path on the given device buffers
+    (the end-to-end leg alternates two buffer sets); step_fn runs it on the
+    resident set, with CUDA events around the dominant kernel when asked."""
     import torch
 
     import synth
@@ -324,52 +328,44 @@ def make_step(wl, dev):
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     meta["h2d"] = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     meta["d2h"] = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    meta["host"] = (hq, hk, hv, ho, hl)
+    meta["device"] = (q, k, v, o, lse)
 
     if kind == "decode":
         splits = attn.splitkv_default_splits(B, Hq, Hkv, Nq, Nk, d)
         ws = torch.empty(attn.splitkv_workspace_bytes(B, Hq, Nq, d, splits), dtype=torch.uint8,
                          device=dev)
 
+        def hot(q, k, v, o, lse):
+            attn.attn_fwd_splitkv(q, k, v, num_splits=splits, scale=scale, out=o, lse=lse,
+                                  workspace=ws)
+
         def step(kernel_events=None):
             if kernel_events:
                 kernel_events[0].record()
-            attn.attn_fwd_splitkv(q, k, v, num_splits=splits, scale=scale, out=o, lse=lse,
-                                  workspace=ws)
+            hot(q, k, v, o, lse)
             if kernel_events:
                 kernel_events[1].record()
-
-        def e2e():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            step()
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
         rows = splits * B * Hq * Nq
         # K and V once, Q, O, LSE, and the FP32 partial rows written and read back
         meta["bytes"] = (2 * B * Nk * Hkv * d * 2 + 2 * B * Nq * Hq * d * 2 + B * Hq * Nq * 4
                          + 2 * rows * (d + 1) * 4)
         meta["launches_per_step"] = 2 if splits > 1 else 1
         meta["kernel"] = f"attn_fwd_kernel<split> + splitkv_merge ({splits} splits)"
-        return step, e2e, meta
+        return step, hot, meta
 
     if kind == "bf16":
+        def hot(q, k, v, o, lse):
+            attn.attn_fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+
         def step(kernel_events=None):
             if kernel_events:
                 kernel_events[0].record()
-            attn.attn_fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+            hot(q, k, v, o, lse)
             if kernel_events:
                 kernel_events[1].record()
-
-        def e2e():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            attn.attn_fwd(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
         meta["launches_per_step"] = 1
-        return step, e2e, meta
+        return step, hot, meta
 
     had = kind in ("fp8h", "fp8hr")
     rope = kind == "fp8hr"
@@ -388,7 +384,7 @@ def make_step(wl, dev):
 
     prep_ev = []   # (start, end) events around the three prep calls of each timed step
 
-    def step(kernel_events=None):
+    def hot(q, k, v, o, lse, kernel_events=None):
         if kernel_events:
             pe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             pe[0].record()
@@ -409,13 +405,8 @@ def make_step(wl, dev):
         if kernel_events:
             kernel_events[1].record()
 
-    def e2e():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+    def step(kernel_events=None):
+        hot(q, k, v, o, lse, kernel_events)
     meta["launches_per_step"] = 4
     meta["kernel"] = "attn_fwd_kernel<e4m3>"
     meta["prep_events"] = prep_ev
@@ -424,7 +415,72 @@ def make_step(wl, dev):
     if rope:
         # the cos / sin tables, read once for Q and once for K
         meta["prep_bytes"] += 2 * (rcos.numel() + rsin.numel()) * 4
-    return step, e2e, meta
+    return step, hot, meta
+
+
+class E2EPipeline:
+    """End-to-end steps through the public API with host buffers: each step
+    copies its inputs from pinned host memory to the device, runs the whole
+    path, and copies the output and LSE back.  Two device buffer sets and
+    separate copy streams let step i+1's upload and step i-1's download
+    overlap step i's kernels; every step's copies stay inside the timed
+    region, which ends after the last download."""
+
+    def __init__(self, hot, host, device, stream):
+        import torch
+        self.torch = torch
+        self.hot = hot
+        self.host = host
+        q, k, v, o, lse = device
+        self.sets = [device, tuple(torch.empty_like(t) for t in (q, k, v, o, lse))]
+        self.comp = stream
+        self.up = torch.cuda.Stream(device=q.device)
+        self.down = torch.cuda.Stream(device=q.device)
+
+    def run(self, n):
+        """Run n steps; return their total time in ms (CUDA events)."""
+        torch = self.torch
+        hq, hk, hv, ho, hl = self.host
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(self.comp)
+        self.up.wait_event(start)
+        self.down.wait_event(start)
+        uploaded, computed, downloaded = [None] * n, [None] * n, [None] * n
+
+        def upload(i):
+            q, k, v, _, _ = self.sets[i % 2]
+            with torch.cuda.stream(self.up):
+                if i >= 2:
+                    self.up.wait_event(computed[i - 2])   # set i % 2 no longer read
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                uploaded[i] = ev()
+                uploaded[i].record(self.up)
+
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            q, k, v, o, lse = self.sets[i % 2]
+            self.comp.wait_event(uploaded[i])
+            if i >= 2:
+                self.comp.wait_event(downloaded[i - 2])   # o, lse of this set read back
+            with torch.cuda.stream(self.comp):
+                self.hot(q, k, v, o, lse)
+            computed[i] = ev()
+            computed[i].record(self.comp)
+            with torch.cuda.stream(self.down):
+                self.down.wait_event(computed[i])
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
+                downloaded[i] = ev()
+                downloaded[i].record(self.down)
+        self.comp.wait_event(downloaded[n - 1])
+        end.record(self.comp)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
 
 
 def gpu_arm(args, rank, world, local):
@@ -434,7 +490,7 @@ def gpu_arm(args, rank, world, local):
     attn.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = args.workload
-    step, e2e, meta = make_step(wl, dev)
+    step, hot, meta = make_step(wl, dev)
     stream = torch.cuda.current_stream()
     flops = meta["flops"]
 
@@ -476,18 +532,12 @@ def gpu_arm(args, rank, world, local):
 
     # ---- end-to-end: host buffers, copies inside the timed region
     e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        e2e()
+    pipe = E2EPipeline(hot, meta["host"], meta["device"], stream)
+    pipe.run(2)
     torch.cuda.synchronize()
     barrier(world)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e()
-    b.record(stream)
-    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(pipe.run(e2e_steps) / e2e_steps, world)
     barrier(world)
-    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, world)
 
     if rank != 0:
         return
