@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import statistics
 import subprocess
 import sys
 import threading
@@ -561,6 +562,17 @@ def gpu_arm(args, rank, world, local):
     cpu_tf, cpu_rows, cpu_s, cpu_threads = (None, 0, 0.0, 0)
     if not args.no_cpu_baseline:
         cpu_tf, cpu_rows, cpu_s, cpu_threads = time_oracle(wl, budget_s=args.cpu_budget)
+    # the second limiter of the softmax: one exp2 per score on the MUFU units,
+    # 32 per SM per cycle (4 sub-partitions x 8 lanes) at the sampled SM clock
+    B_, Hq_, _, Nq_, Nk_, _, causal_, _ = WORKLOADS[wl]
+    exps = B_ * Hq_ * Nq_ * Nk_ * (0.5 if causal_ else 1.0)
+    sm_hz = (clocks.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    exp_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 32 * sm_hz
+    exp_roofline = None if kind == "decode" else {
+        "bound": "mufu", "achieved": exps / (avg_launch_ms * 1e-3) / 1e9,
+        "peak": exp_peak / 1e9, "unit": "Gexp/s",
+        "frac": exps / (avg_launch_ms * 1e-3) / exp_peak,
+        "peak_source": "SMs x 32 exp2 per cycle x median SM clock"}
     prep = None
     if meta.get("prep_events"):
         pms = [a.elapsed_time(b) for a, b in meta["prep_events"]]
@@ -582,12 +594,15 @@ def gpu_arm(args, rank, world, local):
         "cpu_baseline": None if cpu_tf is None else {
             "value": cpu_tf, "unit": "TFLOPS", "cores": cpu_threads, "kind": "oracle",
             "sample": f"{cpu_rows} random query rows of batch 0, FP64 two-pass oracle, "
-                      f"{cpu_s:.1f} s; TFLOPS-equivalent = 4*keys*d per row"},
+                      f"{cpu_s:.1f} s; TFLOPS-equivalent = 4*keys*d per row",
+            "extrapolated_full_problem_s": flops / (cpu_tf * 1e12)},
+        "exp_roofline": exp_roofline,
         "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                 "h2d_bytes_per_step": meta["h2d"], "d2h_bytes_per_step": meta["d2h"]},
         "gpu_launches": launches,
         "prep_roofline": prep,
-        "kernel_ms": {"avg": avg_launch_ms, "min": min(per_launch_ms), "max": max(per_launch_ms)},
+        "kernel_ms": {"avg": avg_launch_ms, "median": statistics.median(per_launch_ms),
+                      "min": min(per_launch_ms), "max": max(per_launch_ms)},
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "status": status,
         "kernel_source_hash": kernel_source_hash(),
