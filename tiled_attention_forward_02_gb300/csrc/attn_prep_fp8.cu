@@ -96,15 +96,6 @@ enum PrepMode : int {
   kPrepTensor = 2,      // per-tensor, second pass: codes from the tensor amax
 };
 
-template <int VEC>
-__device__ __forceinline__ void load_f32(const float* src, float (&t)[VEC]) {
-#pragma unroll
-  for (int q = 0; q < VEC / 4; ++q) {
-    const float4 w = __ldg(reinterpret_cast<const float4*>(src) + q);
-    t[4 * q] = w.x; t[4 * q + 1] = w.y; t[4 * q + 2] = w.z; t[4 * q + 3] = w.w;
-  }
-}
-
 template <int D, int MODE, bool ROPE>
 __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     prep_fp8_kernel(const __grid_constant__ CUtensorMap tmX, uint8_t* __restrict__ x8,
