@@ -58,6 +58,17 @@ def test_splitkv_decode_128k_every_row(gpu_lib):
     assert_within(errors(o, lse, o_ref, lse_ref))
 
 
+def test_splitkv_decode_1m_keys_every_row(gpu_lib):
+    """One query per head against 1,048,576 keys (B=1, Hq=8, Hkv=1, d=128): a
+    million-token context, default split count, every row against the oracle."""
+    q, k, v = synth.attn_inputs(1, 1, 1 << 20, 8, 1, 128, dtype=torch.bfloat16, seed=17,
+                                device="cuda")
+    o, lse = gpu_lib.attn_fwd_splitkv(q, k, v)
+    assert gpu_lib.get_status() == 0
+    o_ref, lse_ref = oracle_for(q, k, v, False, 1 / math.sqrt(128))
+    assert_within(errors(o, lse, o_ref, lse_ref))
+
+
 def test_splitkv_rejects_small_workspace(gpu_lib):
     q, k, v = _inputs(1, 4, 4096, 2, 2, 128, seed=15)
     need = gpu_lib.splitkv_workspace_bytes(1, 2, 4, 128, 8)
