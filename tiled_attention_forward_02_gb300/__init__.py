@@ -4,6 +4,7 @@ The computation runs in hand-written CUDA kernels behind a C ABI
 (``include/attn.h``); this package holds the sources (``csrc/``), the nvcc
 build (``build.py``) and a thin ctypes binding (``attn.py``).
 """
-from .attn import (AttnError, attn_fwd, attn_fwd_fp8, attn_prep_fp8,  # noqa: F401
-                   attn_prep_fp8_per_tensor, attn_prep_fp8_rope, attn_rope_table, get_status,
-                   launch_count, load, strerror)
+from .attn import (AttnError, attn_fwd, attn_fwd_fp8, attn_fwd_splitkv,  # noqa: F401
+                   attn_prep_fp8, attn_prep_fp8_per_tensor, attn_prep_fp8_rope, attn_rope_table,
+                   get_status, launch_count, load, splitkv_default_splits,
+                   splitkv_workspace_bytes, strerror)
