@@ -47,6 +47,9 @@ WORKLOADS = {
     # one query per head against a long key cache: split key ranges + LSE merge
     "bf16_decode_splitkv_B1_Hq64_Hkv8_Nq1_Nk131072_d128": (1, 64, 8, 1, 131072, 128, False,
                                                           "decode"),
+    # a batch of sequences, one new query each, against 8192 cached keys
+    "bf16_decode_batched_B32_Hq64_Hkv8_Nq1_Nk8192_d128": (32, 64, 8, 1, 8192, 128, False,
+                                                          "decode"),
 }
 DEFAULT_WORKLOAD = "bf16_mha_B4_H16_N4096_d128"
 METRIC = "attention fwd TFLOPS (BF16, FP8) at 1 GB300 and % of dense tensor-core peak"
@@ -347,12 +350,14 @@ def make_step(wl, dev):
             hot(q, k, v, o, lse)
             if kernel_events:
                 kernel_events[1].record()
-        rows = splits * B * Hq * Nq
-        # K and V once, Q, O, LSE, and the FP32 partial rows written and read back
+        rows = splits * B * Hq * Nq if splits > 1 else 0
+        # K and V once, Q, O, LSE, and (with several splits) the FP32 partial
+        # rows written and read back
         meta["bytes"] = (2 * B * Nk * Hkv * d * 2 + 2 * B * Nq * Hq * d * 2 + B * Hq * Nq * 4
                          + 2 * rows * (d + 1) * 4)
         meta["launches_per_step"] = 2 if splits > 1 else 1
-        meta["kernel"] = f"attn_fwd_kernel<split> + splitkv_merge ({splits} splits)"
+        meta["kernel"] = (f"attn_fwd_kernel<split> + splitkv_merge ({splits} splits)" if splits > 1
+                          else "attn_fwd_kernel<split> (GQA group packed, one split)")
         return step, hot, meta
 
     if kind == "bf16":

@@ -94,3 +94,26 @@ def test_splitkv_group_packing_and_fallback(gpu_lib, Hq, Hkv):
     assert gpu_lib.get_status() == 0
     o_ref, lse_ref = oracle_for(q, k, v, False, 1 / math.sqrt(128))
     assert_within(errors(o, lse, o_ref, lse_ref))
+
+
+@pytest.mark.parametrize("Hq,Hkv,Nq", [(16, 2, 1), (16, 2, 16), (64, 8, 2), (8, 8, 3), (12, 4, 5)])
+def test_splitkv_single_split_packed(gpu_lib, Hq, Hkv, Nq):
+    """With one split, GQA groups that divide 128 still share query tiles when
+    the packed rows fit (the kernel then writes O and LSE itself, without a
+    workspace); other shapes take the plain kernel."""
+    q, k, v = _inputs(3, Nq, 2000, Hq, Hkv, 128, seed=18)
+    o, lse = gpu_lib.attn_fwd_splitkv(q, k, v, num_splits=1)
+    assert gpu_lib.get_status() == 0
+    o_ref, lse_ref = oracle_for(q, k, v, False, 1 / math.sqrt(128))
+    assert_within(errors(o, lse, o_ref, lse_ref))
+
+
+def test_splitkv_batched_decode_every_row(gpu_lib):
+    """A batch of 32 sequences, one query per head each, 8192 cached keys
+    (B=32, Hq=64, Hkv=8, d=128), default split count, every row."""
+    q, k, v = synth.attn_inputs(32, 1, 8192, 64, 8, 128, dtype=torch.bfloat16, seed=19,
+                                device="cuda")
+    o, lse = gpu_lib.attn_fwd_splitkv(q, k, v)
+    assert gpu_lib.get_status() == 0
+    o_ref, lse_ref = oracle_for(q, k, v, False, 1 / math.sqrt(128))
+    assert_within(errors(o, lse, o_ref, lse_ref))

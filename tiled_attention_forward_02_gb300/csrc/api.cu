@@ -323,6 +323,17 @@ extern "C" int attn_prep_fp8_rope(const void* x, void* x8, float* descale, int B
                          st->sm_count, st->status, static_cast<cudaStream_t>(stream));
 }
 
+namespace attn {
+// query heads packed per tile row group by the split instance: a GQA group
+// whose size divides 128, with several splits, or with one split when the
+// packed rows fit the unit's query tiles (decode-like shapes)
+int splitkv_pack(int group, int eff_splits, int64_t Nq, int d) {
+  if (group > 128 || 128 % group != 0) return 1;
+  if (eff_splits > 1) return group;
+  return (int64_t)Nq * group <= (int64_t)fwd_q_tiles(d) * 128 ? group : 1;
+}
+}  // namespace attn
+
 namespace {
 // key tiles per split and the number of non-empty splits for a request
 void split_layout(int64_t Nk, int num_splits, int* split_tiles, int* eff_splits) {
@@ -386,9 +397,11 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
   // the split instance packs a GQA group into the rows of one query tile so
-  // that each key/value head is streamed once per split
+  // that each key/value head is streamed once per split; with one split it
+  // is used for that alone when the packed rows fit the unit's query tiles
+  // (decode-like shapes), and writes O and LSE directly
   const int group = Hq / Hkv;
-  const int pack_g = (eff > 1 && group <= 128 && 128 % group == 0) ? group : 1;
+  const int pack_g = splitkv_pack(group, eff, Nq, d);
   const CUtensorMapDataType tdt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
@@ -414,7 +427,8 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
   p.o_part = o_part;
   p.lse_part = lse_part;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int mode = eff > 1 ? 2 : 0;   // 2: split instance writing partial results
+  // 2: split instance (partial results when eff > 1, else O and LSE directly)
+  const int mode = (eff > 1 || pack_g > 1) ? 2 : 0;
   rc = dtype == ATTN_BF16 ? launch_fwd_bf16(d, mode, mq, mk, mv, p, grid, s)
                           : launch_fwd_f16(d, mode, mq, mk, mv, p, grid, s);
   if (rc != ATTN_OK || eff == 1) return rc;

@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       const bool live = row < p.Nq;
       // l carries the factor 2^PSHIFT of the FP8 instance (0 otherwise)
       const float lse_row = (mi + ptx::lg2(li) - C::PSHIFT) * 0.6931471805599453f;
-      if constexpr (SPLIT) {
+      if (SPLIT && p.n_splits > 1) {
         // partial result of this key range: FP32 O / l and its LSE
         const long long prow = (((long long)U.sp * p.B + U.b) * p.Hq + hrow) * p.Nq + row;
         float* dst = p.o_part + prow * D;

@@ -32,6 +32,9 @@ int launch_fwd_e4m3(int d, int causal, const CUtensorMap& q, const CUtensorMap& 
 // query tiles per work unit of the fused forward (tensor-memory budget)
 inline int fwd_q_tiles(int d) { return d == 256 ? 1 : 2; }
 
+// query heads the split instance packs into a tile's rows (api.cu)
+int splitkv_pack(int group, int eff_splits, int64_t Nq, int d);
+
 // combines split partial results (O / l per split, LSE per split) into o, lse
 int launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, float* lse,
                          int n_splits, int B, int Hq, int Nq, int d, int dtype, int sm_count,

@@ -130,7 +130,7 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   if (rc != ATTN_OK) return rc;
   const int qst = fwd_q_tiles(d);
   const int group = Hq / Hkv;
-  const int pack_g = (eff > 1 && group <= 128 && 128 % group == 0) ? group : 1;
+  const int pack_g = splitkv_pack(group, eff, Nq, d);
   const int64_t n_mb = (Nq * pack_g + qst * 128 - 1) / (qst * 128);
   const int64_t units = (int64_t)B * (Hq / pack_g) * n_mb * eff;
   if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
@@ -169,7 +169,7 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   p.lse_part = eff > 1 ? lse_part : nullptr;
   const int grid = (int)(units < st->sm_count ? units : st->sm_count);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int mode = eff > 1 ? 2 : 0;
+  const int mode = (eff > 1 || pack_g > 1) ? 2 : 0;
   rc = dtype == ATTN_BF16 ? launch_fwd_bf16(d, mode, mq, mk, mv, p, grid, s)
                           : launch_fwd_f16(d, mode, mq, mk, mv, p, grid, s);
   if (rc != ATTN_OK || eff == 1) return rc;
