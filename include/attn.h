@@ -222,7 +222,9 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t, const float* q
  * key/value head is read once per split.  Same tensors, layouts and results
  * as attn_fwd with causal = 0 (up to FP32 rounding of the merge).
  *   num_splits  >= 1; more splits than 128-key tiles are reduced to one per
- *               tile; an effective count of 1 runs attn_fwd's kernel alone
+ *               tile; with an effective count of 1 the kernel writes O and
+ *               LSE itself (GQA group still packed when Nq x Hq/Hkv fits two
+ *               query tiles, 128 rows for d = 256)
  *   workspace   device buffer, 256-byte aligned, owned by the caller, at least
  *               attn_splitkv_workspace_bytes(B, Hq, Nq, d, num_splits) bytes;
  *               unused (may be NULL) when the effective count is 1.  Its
