@@ -86,7 +86,9 @@ extern "C" {
  *   dtype  ATTN_F16 or ATTN_BF16
  * Arithmetic: products accumulate in FP32 (tensor memory); the softmax state
  * (row max, row sum) is FP32; the probabilities are rounded to dtype before
- * the P V product.
+ * the P V product.  Non-causal calls whose query rows of a GQA group fit two
+ * 128-row tiles (one for d = 256) run with that group's heads packed into
+ * the tiles' rows (same results, one K/V stream per group).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
              int Hkv, int64_t Nq, int64_t Nk, int d, int causal, float scale, int dtype,

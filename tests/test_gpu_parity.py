@@ -51,6 +51,15 @@ def test_unequal_lengths_and_edges(gpu_lib, Nq, Nk, causal):
     assert_within(_run(gpu_lib, 1, Nq, Nk, 8, 1, 128, causal, "bf16", seed=2))
 
 
+@pytest.mark.parametrize("Nq,Hq,Hkv,d", [(16, 64, 8, 128), (32, 16, 2, 128), (5, 32, 4, 64),
+                                          (12, 16, 2, 256), (3, 48, 16, 128)])
+def test_few_queries_gqa_packed(gpu_lib, Nq, Hq, Hkv, d):
+    """Non-causal, few query rows per head: when a GQA group divides 128 and
+    its rows fit the unit's query tiles, the heads of the group share tile
+    rows (one K/V stream per group); a group of 3 takes the plain kernel."""
+    assert_within(_run(gpu_lib, 2, Nq, 1500, Hq, Hkv, d, False, "bf16", seed=6))
+
+
 def test_many_heads_small_sequence(gpu_lib):
     """More work units than SMs with tiny sequences (every CTA loops)."""
     assert_within(_run(gpu_lib, 3, 200, 200, 64, 8, 64, True, "bf16", seed=3))

@@ -194,10 +194,14 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
 
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  // few query rows under grouped-query attention (decode-like, non-causal):
+  // the query heads of a group share the rows of a tile (the split instance
+  // with one split), so each key/value head is streamed once per group
+  const int pack_g = causal ? 1 : splitkv_pack(Hq / Hkv, 1, Nq, d);
   const CUtensorMapDataType tdt =
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
-  if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64)) ||
+  if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64, pack_g)) ||
       (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64)) ||
       (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64)))
     return rc;
@@ -205,10 +209,12 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.o = o;
   p.lse = lse;
   int grid = 0;
-  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid)) != ATTN_OK) return rc;
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid, 1, 0, pack_g)) != ATTN_OK)
+    return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return dtype == ATTN_BF16 ? launch_fwd_bf16(d, causal, mq, mk, mv, p, grid, s)
-                            : launch_fwd_f16(d, causal, mq, mk, mv, p, grid, s);
+  const int mode = pack_g > 1 ? 2 : causal;
+  return dtype == ATTN_BF16 ? launch_fwd_bf16(d, mode, mq, mk, mv, p, grid, s)
+                            : launch_fwd_f16(d, mode, mq, mk, mv, p, grid, s);
 }
 
 extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
