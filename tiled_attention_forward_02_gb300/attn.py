@@ -111,6 +111,16 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be contiguous (BSHD)")
 
 
+def _check_outputs(q, out, lse):
+    """Caller-provided outputs must match what the kernels write."""
+    B, Nq, Hq, _ = q.shape
+    _need_cuda(out, lse)
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must have the shape and dtype of q")
+    if tuple(lse.shape) != (B, Hq, Nq) or lse.dtype != torch.float32:
+        raise ValueError("lse must be float32 [B, Hq, Nq]")
+
+
 def fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, Hq, Hkv, Nq, Nk, d, causal, scale, dtype,
             stream) -> int:
     """Direct C call with raw integers (used by the boundary tests)."""
@@ -135,6 +145,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _check_outputs(q, out, lse)
     dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F16
     rc = load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                          int(bool(causal)), float(scale), dt, _stream(stream))
@@ -169,13 +180,15 @@ def attn_fwd_splitkv(q, k, v, num_splits: int | None = None, scale: float | None
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
-    nbytes = splitkv_workspace_bytes(B, Hq, Nq, d, num_splits)
-    if workspace is None:
+    _check_outputs(q, out, lse)
+    if workspace is None and num_splits > 1:
+        nbytes = splitkv_workspace_bytes(B, Hq, Nq, d, num_splits)
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F16
     rc = load().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq,
                                  Nk, d, int(num_splits), float(scale), dt, _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _stream(stream))
+                                 ws_bytes, _stream(stream))
     _check(rc, "attn_fwd_splitkv")
     return out, lse
 
@@ -276,6 +289,11 @@ def attn_fwd_fp8(q8, k8, v8t, q_descale, k_descale, v_descale, *, Hq: int | None
         out = torch.empty((B, Nq, Hq_, d), dtype=torch.bfloat16, device=q8.device)
     if lse is None:
         lse = torch.empty((B, Hq_, Nq), dtype=torch.float32, device=q8.device)
+    _need_cuda(out, lse)
+    if tuple(out.shape) != (B, Nq, Hq_, d) or out.dtype != torch.bfloat16:
+        raise ValueError("out must be bfloat16 [B, Nq, Hq, d]")
+    if tuple(lse.shape) != (B, Hq_, Nq) or lse.dtype != torch.float32:
+        raise ValueError("lse must be float32 [B, Hq, Nq]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     rc = load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8t), _ptr(q_descale), _ptr(k_descale),
