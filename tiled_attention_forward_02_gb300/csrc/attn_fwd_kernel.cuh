@@ -240,6 +240,30 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, con
   return __all_sync(0xffffffffu, ok);
 }
 
+// 8 x 8 transpose of 16-byte pieces (w[4k .. 4k+3] = piece k) inside each
+// octet of lanes: afterwards piece k of lane 8g + i is what piece i of lane
+// 8g + k was. Three butterfly stages, each swapping the off-diagonal 4 x 4,
+// 2 x 2 and 1 x 1 blocks of pieces between lanes that differ in one bit.
+__device__ __forceinline__ void octet_transpose(uint32_t (&w)[32], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k & m) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t send = hi ? w[4 * k + e] : w[4 * (k | m) + e];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        if (hi)
+          w[4 * k + e] = recv;
+        else
+          w[4 * (k | m) + e] = recv;
+      }
+    }
+  }
+}
+
 // --------------------------------------------------------------------- kernel
 template <int D, int DT, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
@@ -651,43 +675,78 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       const bool live = row < p.Nq;
       // l carries the factor 2^PSHIFT of the FP8 instance (0 otherwise)
       const float lse_row = (mi + ptx::lg2(li) - C::PSHIFT) * 0.6931471805599453f;
-      if (SPLIT && p.n_splits > 1) {
-        // partial result of this key range: FP32 O / l and its LSE
-        const long long prow = (((long long)U.sp * p.B + U.b) * p.Hq + hrow) * p.Nq + row;
-        float* dst = p.o_part + prow * D;
+      if constexpr (SPLIT) {
+        // split instances (few query rows, packed heads): one lane stores its row
+        if (p.n_splits > 1) {
+          // partial result of this key range: FP32 O / l and its LSE
+          const long long prow = (((long long)U.sp * p.B + U.b) * p.Hq + hrow) * p.Nq + row;
+          float* dst = p.o_part + prow * D;
 #pragma unroll 1
-        for (int cb = 0; cb < D; cb += 32) {
-          uint32_t o32[32];
-          ptx::tmem_ld_x32(tO + cb, o32);
-          if (live) {
-            float4* d4 = reinterpret_cast<float4*>(dst + cb);
+          for (int cb = 0; cb < D; cb += 32) {
+            uint32_t o32[32];
+            ptx::tmem_ld_x32(tO + cb, o32);
+            if (live) {
+              float4* d4 = reinterpret_cast<float4*>(dst + cb);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              d4[c] = make_float4(__uint_as_float(o32[4 * c]) * inv, __uint_as_float(o32[4 * c + 1]) * inv,
-                                  __uint_as_float(o32[4 * c + 2]) * inv,
-                                  __uint_as_float(o32[4 * c + 3]) * inv);
+              for (int c = 0; c < 8; ++c)
+                d4[c] = make_float4(__uint_as_float(o32[4 * c]) * inv, __uint_as_float(o32[4 * c + 1]) * inv,
+                                    __uint_as_float(o32[4 * c + 2]) * inv,
+                                    __uint_as_float(o32[4 * c + 3]) * inv);
+            }
           }
+          if (live) p.lse_part[prow] = lse_row;
+        } else {
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                           (((long long)U.b * p.Nq + row) * p.Hq + hrow) * D;
+#pragma unroll 1
+          for (int cb = 0; cb < D; cb += 32) {
+            uint32_t o32[32];
+            ptx::tmem_ld_x32(tO + cb, o32);
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const float a = __uint_as_float(o32[2 * c]) * inv;
+              const float b = __uint_as_float(o32[2 * c + 1]) * inv;
+              pk[c] = (DT == DT_F16) ? ptx::pack_f16x2(a, b) : ptx::pack_bf16x2(a, b);
+            }
+            if (live) {
+              uint4* d4 = reinterpret_cast<uint4*>(orow + cb);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                d4[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            }
+          }
+          if (live) p.lse[((long long)U.b * p.Hq + hrow) * p.Nq + row] = lse_row;
         }
-        if (live) p.lse_part[prow] = lse_row;
       } else {
-        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                         (((long long)U.b * p.Nq + row) * p.Hq + hrow) * D;
+        // Full query tiles: a row-per-lane store would write 16 bytes into each
+        // of 32 rows (32 cache lines) per instruction. After an 8 x 8 transpose
+        // of 16-byte pieces inside each lane octet, lane 8g + i holds piece i of
+        // the rows 8g .. 8g + 7 of this warp, so each store instruction writes
+        // four whole 128-byte lines.
+        const int rb = 32 * quarter + 8 * (lane >> 3);   // first tile row of this lane's octet
+        const int pc = lane & 7;                          // 16-byte piece stored by this lane
+        uint16_t* obase = reinterpret_cast<uint16_t*>(p.o);
 #pragma unroll 1
-        for (int cb = 0; cb < D; cb += 32) {
-          uint32_t o32[32];
-          ptx::tmem_ld_x32(tO + cb, o32);
-          uint32_t pk[16];
+        for (int cb = 0; cb < D; cb += 64) {   // 64 columns = 128 bytes of a row
+          uint32_t o64[64];
+          ptx::tmem_ld_x64(tO + cb, o64);
+          uint32_t w[32];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float a = __uint_as_float(o32[2 * c]) * inv;
-            const float b = __uint_as_float(o32[2 * c + 1]) * inv;
-            pk[c] = (DT == DT_F16) ? ptx::pack_f16x2(a, b) : ptx::pack_bf16x2(a, b);
+          for (int c = 0; c < 32; ++c) {
+            const float a = __uint_as_float(o64[2 * c]) * inv;
+            const float b = __uint_as_float(o64[2 * c + 1]) * inv;
+            w[c] = (DT == DT_F16) ? ptx::pack_f16x2(a, b) : ptx::pack_bf16x2(a, b);
           }
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cb);
+          octet_transpose(w, lane);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          for (int k = 0; k < 8; ++k) {
+            const int pos = m_s + rb + k;
+            if (pos < p.Nq) {
+              uint16_t* dst = obase + (((long long)U.b * p.Nq + pos) * p.Hq + hrow) * D + cb;
+              reinterpret_cast<uint4*>(dst)[pc] =
+                  make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            }
           }
         }
         if (live) p.lse[((long long)U.b * p.Hq + hrow) * p.Nq + row] = lse_row;
