@@ -557,38 +557,46 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         ++s_cnt;
         if (!ok) break;
         ptx::tc_fence_after();
+        // full tiles: the row maximum comes with the TMEM load (tcgen05.ld.red);
+        // a tile with masked keys (causal diagonal, ragged key tail) takes the
+        // maximum of its unmasked logits after the mask instead. Long runs of
+        // max instructions on the softmax warps also take the issue slots the
+        // MMA-issuing thread needs.
+        const int n0 = (U.j0 + j) * 128;
+        const bool masked = (n0 + 128 > p.Nk) || (CAUSAL && n0 + 127 > m_s);
         uint32_t sr[128];
-        ptx::tmem_ld_x128(tS, sr);
+        float rmax;
+        if (!masked) ptx::tmem_ld_max_x128(tS, sr, rmax);
+        else ptx::tmem_ld_x128(tS, sr);
         float sv[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
 
-        const int n0 = (U.j0 + j) * 128;
-        if ((n0 + 128 > p.Nk) || (CAUSAL && n0 + 127 > m_s)) {
+        if (masked) {
           int lim = p.Nk - n0;
           if (CAUSAL) lim = min(lim, row - n0 + 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c) sv[c] = (c < lim) ? sv[c] : -CUDART_INF_F;
+          // 16 independent chains of 3-input max, then a tree
+          float mx[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            mx[i] = ptx::max3(sv[i], sv[i + 16], sv[i + 32]);
+            mx[i] = ptx::max3(mx[i], sv[i + 48], sv[i + 64]);
+            mx[i] = ptx::max3(mx[i], sv[i + 80], sv[i + 96]);
+            mx[i] = fmaxf(mx[i], sv[i + 112]);
+          }
+          const float mxa = ptx::max3(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], mx[5]),
+                                      ptx::max3(mx[6], mx[7], mx[8]));
+          const float mxb = ptx::max3(ptx::max3(mx[9], mx[10], mx[11]),
+                                      ptx::max3(mx[12], mx[13], mx[14]), mx[15]);
+          rmax = fmaxf(mxa, mxb);
         }
 
         const float cj = cj_cur;           // logit scale of this tile (log2 units)
         const float bias_extra = bias_cur; // FP8: exponent shift and V-block factor
         const float sum_scale = ssc_cur;   // FP8: converts the tile's row sum back to unit P
-
-        // row max of this tile: 16 independent chains of 3-input max, then a tree
-        float mx[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          mx[i] = ptx::max3(sv[i], sv[i + 16], sv[i + 32]);
-          mx[i] = ptx::max3(mx[i], sv[i + 48], sv[i + 64]);
-          mx[i] = ptx::max3(mx[i], sv[i + 80], sv[i + 96]);
-          mx[i] = fmaxf(mx[i], sv[i + 112]);
-        }
-        const float mxa = ptx::max3(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], mx[5]),
-                                    ptx::max3(mx[6], mx[7], mx[8]));
-        const float mxb = ptx::max3(ptx::max3(mx[9], mx[10], mx[11]),
-                                    ptx::max3(mx[12], mx[13], mx[14]), mx[15]);
-        const float mj = fmaxf(mxa, mxb) * cj;
+        const float mj = rmax * cj;
         const float m_new = fmaxf(mi, mj);
         float alpha = 1.f;
         bool rescale = false;
