@@ -132,6 +132,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor split into words: the high word (stride byte offset
+// 1024, version, 128-byte swizzle) is the same for every operand here, and the
+// start address is the low 14 bits of the low word in 16-byte units. Shared
+// memory offsets stay below 2^18 bytes, so adding (offset >> 4) to the low
+// word never carries out of the field: one add per MMA operand.
+constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sdesc_of(uint32_t lo) {
+  return ((uint64_t)kSdescHi << 32) | lo;
+}
+
 // tcgen05 instruction descriptor: FP32 accumulate, dense, A K-major.
 // fmt: 0 = f16 / e4m3, 1 = bf16 / e5m2 (per kind); b_mn_major selects a
 // transposed (N-contiguous) B operand.
@@ -440,17 +453,33 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
               if (!ok) break;
               ptx::tc_fence_after();
               const uint32_t vbase = sKV + vslot * C::KVBYTES;
-              if constexpr (DT == DT_E4M3) {
+              if constexpr (SPLIT) {
+                // (the split instances' issuing thread has no registers to spare
+                // for the precomputed descriptor words)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)   // 32 keys per MMA, 8 TMEM columns of P
-                  ptx::mma_f8_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 32, 16, 1024), idO,
-                                 (j > 1 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < (DT == DT_E4M3 ? 4 : 8); ++kk) {
+                  if constexpr (DT == DT_E4M3)
+                    ptx::mma_f8_ts(tO, tS + kk * 8, sdesc_sw128(vbase + kk * 32, 16, 1024), idO,
+                                   (j > 1 || kk > 0) ? 1u : 0u);
+                  else
+                    ptx::mma_f16_ts(tO, tS + kk * 8,
+                                    sdesc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), idO,
+                                    (j > 1 || kk > 0) ? 1u : 0u);
+                }
+              } else if constexpr (DT == DT_E4M3) {
+                // 32 keys per MMA, 8 TMEM columns of P
+                const uint32_t vlo = sdesc_lo(vbase, 16);
+                ptx::mma_f8_ts(tO, tS, sdesc_of(vlo), idO, j > 1 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 1; kk < 4; ++kk)
+                  ptx::mma_f8_ts_c<1>(tO, tS + kk * 8, sdesc_of(vlo + kk * (32 >> 4)), idO);
               } else {
+                // 16 keys per MMA, 8 TMEM columns of P
+                const uint32_t vlo = sdesc_lo(vbase, C::CHUNK_BYTES);
+                ptx::mma_f16_ts(tO, tS, sdesc_of(vlo), idO, j > 1 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)   // 16 keys per MMA, 8 TMEM columns of P
-                  ptx::mma_f16_ts(tO, tS + kk * 8,
-                                  sdesc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), idO,
-                                  (j > 1 || kk > 0) ? 1u : 0u);
+                for (int kk = 1; kk < 8; ++kk)
+                  ptx::mma_f16_ts_c<1>(tO, tS + kk * 8, sdesc_of(vlo + kk * (2048 >> 4)), idO);
               }
               if (j - 1 == U.n_s[s] - 1) ptx::tc_commit(bar(B_OFULL + s));
               // the last active query tile visits every key tile: it is the last reader
@@ -467,15 +496,35 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
               const uint32_t qbase = sQ + s * C::QBYTES;
               const uint32_t kbase = sKV + kslot * C::KVBYTES;
               constexpr int KSTEPS = C::ROWB / 32;   // 32 bytes of K per MMA
+              if constexpr (SPLIT) {
+                // (the split instances' issuing thread has no registers to spare
+                // for the precomputed descriptor words)
 #pragma unroll
-              for (int kk = 0; kk < KSTEPS; ++kk) {
-                const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-                const uint64_t a = sdesc_sw128(qbase + off, 16, 1024);
-                const uint64_t b = sdesc_sw128(kbase + off, 16, 1024);
-                if constexpr (DT == DT_E4M3)
-                  ptx::mma_f8_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
-                else
-                  ptx::mma_f16_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                  const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+                  const uint64_t a = sdesc_sw128(qbase + off, 16, 1024);
+                  const uint64_t b = sdesc_sw128(kbase + off, 16, 1024);
+                  if constexpr (DT == DT_E4M3)
+                    ptx::mma_f8_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
+                  else
+                    ptx::mma_f16_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
+                }
+              } else {
+                const uint32_t qlo = sdesc_lo(qbase, 16);
+                const uint32_t klo = sdesc_lo(kbase, 16);
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                  const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
+                  const uint64_t a = sdesc_of(qlo + off);
+                  const uint64_t b = sdesc_of(klo + off);
+                  if constexpr (DT == DT_E4M3) {
+                    if (kk == 0) ptx::mma_f8_ss_c<0>(tS, a, b, idS);
+                    else ptx::mma_f8_ss_c<1>(tS, a, b, idS);
+                  } else {
+                    if (kk == 0) ptx::mma_f16_ss_c<0>(tS, a, b, idS);
+                    else ptx::mma_f16_ss_c<1>(tS, a, b, idS);
+                  }
+                }
               }
               ptx::tc_commit(bar(B_SFULL + s));
               if (s == s_last) ptx::tc_commit(bar(B_KVEMPTY + kslot));
