@@ -42,6 +42,8 @@
 #include <math_constants.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "ptx.cuh"
 
 namespace attn {
@@ -143,6 +145,27 @@ __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
 }
 __device__ __forceinline__ uint64_t sdesc_of(uint32_t lo) {
   return ((uint64_t)kSdescHi << 32) | lo;
+}
+
+// S = Q K^T: one MMA per 32 bytes of the head dimension; the operands' low
+// descriptor words advance by the same offset in Q and K (16-byte units)
+template <int DT, int CHUNK_BYTES, size_t... KK>
+__device__ __forceinline__ void issue_s_mmas(uint32_t tS, uint32_t qlo, uint32_t klo, uint32_t idS,
+                                             std::index_sequence<KK...>) {
+  (ptx::mma_ss_lo<DT == DT_E4M3, (KK > 0 ? 1 : 0),
+                  (uint32_t)((((int)KK >> 2) * CHUNK_BYTES + ((int)KK & 3) * 32) >> 4), kSdescHi>(
+       tS, qlo, klo, idS),
+   ...);
+}
+// O += P V with P read from tensor memory (8 columns per MMA) and the V tile
+// advancing by VSTEP bytes per MMA
+// advancing by VSTEP bytes per MMA; FIRST: the unit's first PV overwrites O
+template <int DT, int VSTEP, bool FIRST, size_t... KK>
+__device__ __forceinline__ void issue_pv_mmas(uint32_t tO, uint32_t tS, uint32_t vlo, uint32_t idO,
+                                              std::index_sequence<KK...>) {
+  (ptx::mma_ts_lo<DT == DT_E4M3, (FIRST && KK == 0) ? 0 : 1, (uint32_t)(KK * 8),
+                  (uint32_t)((KK * VSTEP) >> 4), kSdescHi>(tO, tS, vlo, idO),
+   ...);
 }
 
 // tcgen05 instruction descriptor: FP32 accumulate, dense, A K-major.
@@ -418,6 +441,21 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       constexpr uint32_t fmt = (DT == DT_BF16) ? 1u : 0u;
       constexpr uint32_t idS = idesc_make(fmt, 128, 128, false);
       constexpr uint32_t idO = idesc_make(fmt, 128, D, DT != DT_E4M3);
+      // S = Q K^T into tS and O += P V with P read from tS (accumulating),
+      // from the low descriptor words of the operands' shared-memory tiles
+      auto issue_s = [&](uint32_t tS, uint32_t qlo, uint32_t klo) {
+        issue_s_mmas<DT, C::CHUNK_BYTES>(tS, qlo, klo, idS,
+                                         std::make_index_sequence<C::ROWB / 32>{});
+      };
+      // FP8: 32 keys per MMA (V^T tile, K-major); 16-bit: 16 keys per MMA
+      constexpr int PV_MMAS = DT == DT_E4M3 ? 4 : 8;
+      constexpr int VSTEP = DT == DT_E4M3 ? 32 : 2048;
+      auto issue_pv = [&](uint32_t tO, uint32_t tS, uint32_t vlo) {
+        issue_pv_mmas<DT, VSTEP, false>(tO, tS, vlo, idO, std::make_index_sequence<PV_MMAS>{});
+      };
+      auto issue_pv_first = [&](uint32_t tO, uint32_t tS, uint32_t vlo) {
+        issue_pv_mmas<DT, VSTEP, true>(tO, tS, vlo, idO, std::make_index_sequence<PV_MMAS>{});
+      };
       int kv_it = 0, u_it = 0;
       int pv_cnt[2] = {0, 0};
       bool ok = true;
@@ -432,6 +470,67 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         if (!ok) break;
         ptx::tc_fence_after();
         for (int j = 0; j <= U.n && ok; ++j) {
+          if constexpr (QST == 2 && !SPLIT) {
+            // Steady state: for 2 <= j < min(n_s) - 1 both query tiles take
+            // PV(j-1) and S(j) and none of the unit's first or last steps
+            // (O buffers, Q release, last PV) falls in the range. The issuing
+            // thread shares its sub-partition with two softmax warps and
+            // waits for a scheduler slot on every instruction, so this loop
+            // keeps ring slots and phases as running counters, tests no edge
+            // case and checks the waits' status once per key tile.
+            const int n_both = U.n_s[0] < U.n_s[1] ? U.n_s[0] : U.n_s[1];
+            const int jend = n_both - 1;
+            if (j == 2 && jend > 2) {
+              int vs = (kv_it + 3) % NSLOT;                 // V_{j-1}: ring index kv_it + 2j - 1
+              uint32_t vph = ((kv_it + 3) / NSLOT) & 1;
+              int ks = (kv_it + 4) % NSLOT;                 // K_j: ring index kv_it + 2j
+              uint32_t kph = ((kv_it + 4) / NSLOT) & 1;
+              uint32_t pph0 = pv_cnt[0] & 1, pph1 = pv_cnt[1] & 1;
+              const uint32_t qlo0 = sdesc_lo(sQ, 16);
+              const uint32_t qlo1 = sdesc_lo(sQ + C::QBYTES, 16);
+              const uint32_t tS0 = tmem + C::S_COL0, tS1 = tS0 + 128;
+              const uint32_t tO0 = tmem + C::O_COL0, tO1 = tO0 + D;
+              bool sok = true;
+              for (; j < jend; ++j) {
+                const uint32_t vlo = sdesc_lo(sKV + vs * C::KVBYTES, DT == DT_E4M3 ? 16 : C::CHUNK_BYTES);
+                const uint32_t klo = sdesc_lo(sKV + ks * C::KVBYTES, 16);
+                sok &= wait_bar(bar(B_KVFULL + vs), vph, ctl);
+                sok &= wait_bar(bar(B_PFULL + 0), pph0, ctl);
+                ptx::tc_fence_after();
+                issue_pv(tO0, tS0, vlo);
+                sok &= wait_bar(bar(B_KVFULL + ks), kph, ctl);
+                ptx::tc_fence_after();
+                issue_s(tS0, qlo0, klo);
+                ptx::tc_commit(bar(B_SFULL + 0));
+                sok &= wait_bar(bar(B_PFULL + 1), pph1, ctl);
+                ptx::tc_fence_after();
+                issue_pv(tO1, tS1, vlo);
+                ptx::tc_commit(bar(B_KVEMPTY + vs));
+                issue_s(tS1, qlo1, klo);
+                ptx::tc_commit(bar(B_SFULL + 1));
+                ptx::tc_commit(bar(B_KVEMPTY + ks));
+                pph0 ^= 1u;
+                pph1 ^= 1u;
+                vs = ks + 1;
+                vph = kph;
+                if (vs == NSLOT) {
+                  vs = 0;
+                  vph ^= 1u;
+                }
+                ks = vs + 1;
+                kph = vph;
+                if (ks == NSLOT) {
+                  ks = 0;
+                  kph ^= 1u;
+                }
+                if (!sok) break;
+              }
+              pv_cnt[0] += j - 2;
+              pv_cnt[1] += j - 2;
+              ok = sok;
+              if (!ok) break;
+            }
+          }
           const int k_idx = kv_it + 2 * j;       // ring index of K_j
           const int v_idx = kv_it + 2 * j - 1;   // ring index of V_{j-1}
           const int kslot = k_idx % NSLOT;
@@ -466,20 +565,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                                     sdesc_sw128(vbase + kk * 2048, C::CHUNK_BYTES, 1024), idO,
                                     (j > 1 || kk > 0) ? 1u : 0u);
                 }
-              } else if constexpr (DT == DT_E4M3) {
-                // 32 keys per MMA, 8 TMEM columns of P
-                const uint32_t vlo = sdesc_lo(vbase, 16);
-                ptx::mma_f8_ts(tO, tS, sdesc_of(vlo), idO, j > 1 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 1; kk < 4; ++kk)
-                  ptx::mma_f8_ts_c<1>(tO, tS + kk * 8, sdesc_of(vlo + kk * (32 >> 4)), idO);
               } else {
-                // 16 keys per MMA, 8 TMEM columns of P
-                const uint32_t vlo = sdesc_lo(vbase, C::CHUNK_BYTES);
-                ptx::mma_f16_ts(tO, tS, sdesc_of(vlo), idO, j > 1 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 1; kk < 8; ++kk)
-                  ptx::mma_f16_ts_c<1>(tO, tS + kk * 8, sdesc_of(vlo + kk * (2048 >> 4)), idO);
+                const uint32_t vlo = sdesc_lo(vbase, DT == DT_E4M3 ? 16 : C::CHUNK_BYTES);
+                if (j > 1) issue_pv(tO, tS, vlo);
+                else issue_pv_first(tO, tS, vlo);
               }
               if (j - 1 == U.n_s[s] - 1) ptx::tc_commit(bar(B_OFULL + s));
               // the last active query tile visits every key tile: it is the last reader
@@ -510,21 +599,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                     ptx::mma_f16_ss(tS, a, b, idS, kk > 0 ? 1u : 0u);
                 }
               } else {
-                const uint32_t qlo = sdesc_lo(qbase, 16);
-                const uint32_t klo = sdesc_lo(kbase, 16);
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk) {
-                  const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4;
-                  const uint64_t a = sdesc_of(qlo + off);
-                  const uint64_t b = sdesc_of(klo + off);
-                  if constexpr (DT == DT_E4M3) {
-                    if (kk == 0) ptx::mma_f8_ss_c<0>(tS, a, b, idS);
-                    else ptx::mma_f8_ss_c<1>(tS, a, b, idS);
-                  } else {
-                    if (kk == 0) ptx::mma_f16_ss_c<0>(tS, a, b, idS);
-                    else ptx::mma_f16_ss_c<1>(tS, a, b, idS);
-                  }
-                }
+                issue_s(tS, sdesc_lo(qbase, 16), sdesc_lo(kbase, 16));
               }
               ptx::tc_commit(bar(B_SFULL + s));
               if (s == s_last) ptx::tc_commit(bar(B_KVEMPTY + kslot));

@@ -185,6 +185,50 @@ __device__ __forceinline__ void mma_f8_ts_c(uint32_t d, uint32_t a_tmem, uint64_
                "l"(b), "r"(idesc), "n"(ACC)
                : "memory");
 }
+// The same two MMA forms with each shared-memory descriptor built inside the
+// instruction's own asm block from a low word (register) plus an offset and
+// the high word (immediates): the issuing thread holds one register per
+// operand tile, and nothing can be hoisted out of a loop into registers.
+// F8 selects kind::f8f6f4 (E4M3) over kind::f16; ACC = 0 overwrites D.
+template <bool F8, int ACC, uint32_t OFF, uint32_t HI>
+__device__ __forceinline__ void mma_ss_lo(uint32_t d, uint32_t alo, uint32_t blo, uint32_t idesc) {
+  if constexpr (F8)
+    asm volatile(
+        "{\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "add.u32 al, %1, %4;\n\tadd.u32 bl, %2, %4;\n\t"
+        "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, %6;\n\t}" ::"r"(d),
+        "r"(alo), "r"(blo), "r"(idesc), "n"(OFF), "n"(HI), "n"(ACC)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "add.u32 al, %1, %4;\n\tadd.u32 bl, %2, %4;\n\t"
+        "mov.b64 da, {al, %5};\n\tmov.b64 db, {bl, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, %6;\n\t}" ::"r"(d),
+        "r"(alo), "r"(blo), "r"(idesc), "n"(OFF), "n"(HI), "n"(ACC)
+        : "memory");
+}
+// A from tensor memory at column offset ACOL, B descriptor as above
+template <bool F8, int ACC, uint32_t ACOL, uint32_t OFF, uint32_t HI>
+__device__ __forceinline__ void mma_ts_lo(uint32_t d, uint32_t a_tmem, uint32_t blo, uint32_t idesc) {
+  if constexpr (F8)
+    asm volatile(
+        "{\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+        "add.u32 at, %1, %4;\n\tadd.u32 bl, %2, %5;\n\t"
+        "mov.b64 db, {bl, %6};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [at], db, %3, %7;\n\t}" ::"r"(d),
+        "r"(a_tmem), "r"(blo), "r"(idesc), "n"(ACOL), "n"(OFF), "n"(HI), "n"(ACC)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+        "add.u32 at, %1, %4;\n\tadd.u32 bl, %2, %5;\n\t"
+        "mov.b64 db, {bl, %6};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, %7;\n\t}" ::"r"(d),
+        "r"(a_tmem), "r"(blo), "r"(idesc), "n"(ACOL), "n"(OFF), "n"(HI), "n"(ACC)
+        : "memory");
+}
 // 8-bit float inputs (E4M3/E5M2), FP32 accumulate
 __device__ __forceinline__ void mma_f8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t accumulate) {
