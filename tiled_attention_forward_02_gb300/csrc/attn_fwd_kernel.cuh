@@ -95,9 +95,16 @@ struct FwdCfg {
   static constexpr int KVBYTES = BN * ROWB;         // K tile; V (or V^T) tile is the same size
   static constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
   static constexpr int SMEM_TAIL = 512;             // barriers + TMEM address + flags
-  static constexpr int SLOT_FIT = (SMEM_LIMIT - 1024 - SMEM_TAIL - QST * QBYTES) / KVBYTES;
+  // FP8 with two query tiles: P goes to a shared-memory buffer per query tile
+  // instead of over S in tensor memory, so the next S GEMM of a tile can run
+  // while the softmax of its current key tile still computes P
+  static constexpr bool PSMEM = (DT == DT_E4M3) && (QST == 2);
+  static constexpr int PBYTES = BM * BN * ELT;      // one P tile (K-major, 128-byte swizzle)
+  static constexpr int PTOTAL = PSMEM ? QST * 2 * PBYTES : 0;   // two buffers per query tile
+  static constexpr int SLOT_FIT =
+      (SMEM_LIMIT - 1024 - SMEM_TAIL - QST * QBYTES - PTOTAL) / KVBYTES;
   static constexpr int NSLOT = SLOT_FIT > 8 ? 8 : SLOT_FIT;
-  static constexpr int SMEM_BYTES = 1024 + QST * QBYTES + NSLOT * KVBYTES + SMEM_TAIL;
+  static constexpr int SMEM_BYTES = 1024 + QST * QBYTES + PTOTAL + NSLOT * KVBYTES + SMEM_TAIL;
   static constexpr int TMEM_COLS = 512;
   static constexpr int S_COL0 = 0;                  // S_s at S_COL0 + 128 s
   static constexpr int O_COL0 = 128 * QST;          // O_s at O_COL0 + D s
@@ -149,10 +156,11 @@ __device__ __forceinline__ uint64_t sdesc_of(uint32_t lo) {
 
 // S = Q K^T: one MMA per 32 bytes of the head dimension; the operands' low
 // descriptor words advance by the same offset in Q and K (16-byte units)
-template <int DT, int CHUNK_BYTES, size_t... KK>
+// (ACC0: the first MMA accumulates too; used for O += P V with P in shared memory)
+template <int DT, int CHUNK_BYTES, bool ACC0 = false, size_t... KK>
 __device__ __forceinline__ void issue_s_mmas(uint32_t tS, uint32_t qlo, uint32_t klo, uint32_t idS,
                                              std::index_sequence<KK...>) {
-  (ptx::mma_ss_lo<DT == DT_E4M3, (KK > 0 ? 1 : 0),
+  (ptx::mma_ss_lo<DT == DT_E4M3, ((KK > 0 || ACC0) ? 1 : 0),
                   (uint32_t)((((int)KK >> 2) * CHUNK_BYTES + ((int)KK & 3) * 32) >> 4), kSdescHi>(
        tS, qlo, klo, idS),
    ...);
@@ -313,9 +321,12 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   const uint32_t sraw = ptx::smem_addr(smem_raw);
   const uint32_t pad = (1024u - (sraw & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
+  static_assert(!(C::PSMEM && SPLIT), "split instances keep P in tensor memory");
   const uint32_t sQ = sraw + pad;                       // QST query tiles
-  const uint32_t sKV = sQ + QST * C::QBYTES;            // NSLOT K/V slots
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QST * C::QBYTES + NSLOT * C::KVBYTES);
+  const uint32_t sP = sQ + QST * C::QBYTES;             // P tiles (shared-memory P only)
+  const uint32_t sKV = sP + C::PTOTAL;                  // NSLOT K/V slots
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + QST * C::QBYTES + C::PTOTAL + NSLOT * C::KVBYTES);
 
   // barrier table
   constexpr int B_QFULL = 0;                 // [2]   TMA Q landed            (tx)
@@ -327,7 +338,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   constexpr int B_OFULL = B_PFULL + 2;       // [2]   last PV of unit done    (commit)
   constexpr int B_OEMPTY = B_OFULL + 2;      // [2]   epilogue read O_s       (4 warp arrivals)
   constexpr int B_DRAIN = B_OEMPTY + 2;      // [1]   all MMAs of this CTA done (commit)
-  constexpr int NBARS = B_DRAIN + 1;
+  // shared-memory P only: P buffer b of tile s is entry 2 s + b
+  constexpr int B_SFREE = B_DRAIN + 1;       // [2]   S_s read into registers (4 warp arrivals)
+  constexpr int B_PFULLB = B_SFREE + 2;      // [2x2] P buffer written      (4 warp arrivals)
+  constexpr int B_PFREEB = B_PFULLB + 4;     // [2x2] PV done reading it    (commit)
+  constexpr int NBARS = B_PFREEB + 4;
   static_assert(NBARS * 8 + 16 <= C::SMEM_TAIL, "barrier table too large");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -355,6 +370,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       ptx::mbar_init(bar(B_KVEMPTY + i), 1);
     }
     ptx::mbar_init(bar(B_DRAIN), 1);
+    for (int s = 0; s < 2; ++s) ptx::mbar_init(bar(B_SFREE + s), 4);
+    for (int i = 0; i < 4; ++i) {
+      ptx::mbar_init(bar(B_PFULLB + i), 4);
+      ptx::mbar_init(bar(B_PFREEB + i), 1);
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -456,6 +476,145 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       auto issue_pv_first = [&](uint32_t tO, uint32_t tS, uint32_t vlo) {
         issue_pv_mmas<DT, VSTEP, true>(tO, tS, vlo, idO, std::make_index_sequence<PV_MMAS>{});
       };
+      if constexpr (C::PSMEM) {
+        // P in shared memory (two buffers per query tile): per key tile j the
+        // order is S_0(j), PV_0(j-1), S_1(j), PV_1(j-1). S_s(j) waits only
+        // until the softmax of tile s holds S_s(j-1) in registers, so it runs
+        // while that softmax still computes P_s(j-1); PV reads P from shared
+        // memory and its completion frees the buffer. PV number n of a tile
+        // uses buffer n % 2, whose barriers complete once per two PVs.
+        int kv_it = 0, u_it = 0;
+        int pv_cnt[2] = {0, 0};   // PV GEMMs issued per query tile
+        int sg_cnt[2] = {0, 0};   // S GEMMs issued per query tile
+        bool ok = true;
+        const uint32_t qlo0 = sdesc_lo(sQ, 16);
+        const uint32_t plo0 = sdesc_lo(sP, 16);   // buffer i at plo0 + i * (PBYTES >> 4)
+        auto pv_ss = [&](int s, int n, bool first, uint32_t vlo) {
+          const uint32_t tO = tmem + C::O_COL0 + D * s;
+          const uint32_t plo = plo0 + (uint32_t)(2 * s + (n & 1)) * (C::PBYTES >> 4);
+          if (first)
+            issue_s_mmas<DT, C::CHUNK_BYTES, false>(tO, plo, vlo, idO,
+                                                    std::make_index_sequence<C::BN * C::ELT / 32>{});
+          else
+            issue_s_mmas<DT, C::CHUNK_BYTES, true>(tO, plo, vlo, idO,
+                                                   std::make_index_sequence<C::BN * C::ELT / 32>{});
+          ptx::tc_commit(bar(B_PFREEB + 2 * s + (n & 1)));
+        };
+        for (int it = 0; ok; ++it) {
+          const int u = unit_of_round<CAUSAL>(it, p);
+          if (u == -2) break;
+          if (u < 0) continue;
+          const Unit U = decode_unit<QST, CAUSAL, SPLIT>(u, p);
+          for (int s = 0; s < QST && ok; ++s) ok = wait_bar(bar(B_QFULL + s), u_it & 1, ctl);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const int n_both = U.n_s[0] < U.n_s[1] ? U.n_s[0] : U.n_s[1];
+          const int jend = n_both - 1;
+          for (int j = 0; j <= U.n && ok; ++j) {
+            if (j == 2 && jend > 2) {
+              // steady state: both tiles take S(j) and PV(j-1), no unit edge
+              // step in range; running counters, one status check per tile
+              int vs = (kv_it + 3) % NSLOT;
+              uint32_t vph = ((kv_it + 3) / NSLOT) & 1;
+              int ks = (kv_it + 4) % NSLOT;
+              uint32_t kph = ((kv_it + 4) / NSLOT) & 1;
+              uint32_t sf0 = (sg_cnt[0] - 1) & 1, sf1 = (sg_cnt[1] - 1) & 1;
+              int n0 = pv_cnt[0], n1 = pv_cnt[1];
+              const uint32_t tS0 = tmem + C::S_COL0, tS1 = tS0 + 128;
+              bool sok = true;
+              for (; j < jend; ++j) {
+                const uint32_t klo = sdesc_lo(sKV + ks * C::KVBYTES, 16);
+                const uint32_t vlo = sdesc_lo(sKV + vs * C::KVBYTES, 16);
+                sok &= wait_bar(bar(B_KVFULL + ks), kph, ctl);
+                sok &= wait_bar(bar(B_SFREE + 0), sf0, ctl);
+                ptx::tc_fence_after();
+                issue_s(tS0, qlo0, klo);
+                ptx::tc_commit(bar(B_SFULL + 0));
+                sok &= wait_bar(bar(B_KVFULL + vs), vph, ctl);
+                sok &= wait_bar(bar(B_PFULLB + (n0 & 1)), (n0 >> 1) & 1, ctl);
+                ptx::tc_fence_after();
+                pv_ss(0, n0, false, vlo);
+                sok &= wait_bar(bar(B_SFREE + 1), sf1, ctl);
+                ptx::tc_fence_after();
+                issue_s(tS1, qlo0 + (C::QBYTES >> 4), klo);
+                ptx::tc_commit(bar(B_SFULL + 1));
+                ptx::tc_commit(bar(B_KVEMPTY + ks));
+                sok &= wait_bar(bar(B_PFULLB + 2 + (n1 & 1)), (n1 >> 1) & 1, ctl);
+                ptx::tc_fence_after();
+                pv_ss(1, n1, false, vlo);
+                ptx::tc_commit(bar(B_KVEMPTY + vs));
+                sf0 ^= 1u;
+                sf1 ^= 1u;
+                ++n0;
+                ++n1;
+                vs = ks + 1;
+                vph = kph;
+                if (vs == NSLOT) {
+                  vs = 0;
+                  vph ^= 1u;
+                }
+                ks = vs + 1;
+                kph = vph;
+                if (ks == NSLOT) {
+                  ks = 0;
+                  kph ^= 1u;
+                }
+                if (!sok) break;
+              }
+              sg_cnt[0] += n0 - pv_cnt[0];
+              sg_cnt[1] += n1 - pv_cnt[1];
+              pv_cnt[0] = n0;
+              pv_cnt[1] = n1;
+              ok = sok;
+              if (!ok) break;
+            }
+            const int k_idx = kv_it + 2 * j;       // ring index of K_j
+            const int v_idx = kv_it + 2 * j - 1;   // ring index of V_{j-1}
+            const int kslot = k_idx % NSLOT;
+            const int vslot = (v_idx + NSLOT) % NSLOT;
+            bool k_ready = false, v_ready = false;
+#pragma unroll
+            for (int s = 0; s < QST; ++s) {
+              if (j < U.n_s[s]) {
+                // S_s = Q_s K_j^T once the softmax holds S_s(j-1)
+                if (!k_ready) {
+                  ok = wait_bar(bar(B_KVFULL + kslot), (k_idx / NSLOT) & 1, ctl);
+                  k_ready = true;
+                }
+                if (ok && sg_cnt[s] > 0) ok = wait_bar(bar(B_SFREE + s), (sg_cnt[s] - 1) & 1, ctl);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                issue_s(tmem + C::S_COL0 + 128 * s, qlo0 + (uint32_t)s * (C::QBYTES >> 4),
+                        sdesc_lo(sKV + kslot * C::KVBYTES, 16));
+                ptx::tc_commit(bar(B_SFULL + s));
+                ++sg_cnt[s];
+                // the second query tile visits every key tile: it is the last reader
+                if (s == QST - 1) ptx::tc_commit(bar(B_KVEMPTY + kslot));
+              }
+              if (j >= 1 && j - 1 < U.n_s[s]) {
+                // O_s += P_s V_{j-1}, P_s from shared memory
+                if (!v_ready) {
+                  ok = wait_bar(bar(B_KVFULL + vslot), (v_idx / NSLOT) & 1, ctl);
+                  v_ready = true;
+                }
+                const int n = pv_cnt[s];
+                if (ok) ok = wait_bar(bar(B_PFULLB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
+                if (ok && j == 1) ok = wait_bar(bar(B_OEMPTY + s), (u_it & 1) ^ 1, ctl);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                pv_ss(s, n, j == 1, sdesc_lo(sKV + vslot * C::KVBYTES, 16));
+                ++pv_cnt[s];
+                if (j - 1 == U.n_s[s] - 1) ptx::tc_commit(bar(B_OFULL + s));
+                if (s == QST - 1) ptx::tc_commit(bar(B_KVEMPTY + vslot));
+              }
+            }
+            if (!ok) break;
+            if (j == U.n - 1) ptx::tc_commit(bar(B_QEMPTY));
+          }
+          kv_it += 2 * U.n;
+          ++u_it;
+        }
+      } else {
       int kv_it = 0, u_it = 0;
       int pv_cnt[2] = {0, 0};
       bool ok = true;
@@ -611,6 +770,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         kv_it += 2 * U.n;
         ++u_it;
       }
+      }
       // every MMA issued by this thread must finish before TMEM is released
       ptx::tc_commit(bar(B_DRAIN));
       wait_bar(bar(B_DRAIN), 0, Ctl{abort_flag, p.status});
@@ -626,6 +786,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     const uint32_t tS = tmem + lane_off + C::S_COL0 + 128 * s;
     const uint32_t tO = tmem + lane_off + C::O_COL0 + D * s;
     int s_cnt = 0, u_it = 0;
+    int p_cnt = 0;   // P tiles this warpgroup has handed to the MMA thread
+    // shared-memory P: this thread's row of the tile's P buffer (K-major,
+    // 128-byte swizzle: 8-row groups of 1024 bytes, 128 bytes per row)
+    const uint32_t prow0 = sP + 2 * s * C::PBYTES + (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = true;
     // a query tile that holds no rows in this launch (Nq <= 128) does nothing
     for (int it = 0; ok && s < n_active; ++it) {
@@ -663,11 +827,16 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       // the softmax critical path
       float cj_cur = p.scale_log2, bias_cur = 0.f, ssc_cur = 1.f;
       float kd_next = 1.f, vd_next = 1.f;
+      // (no divisions: with the softmax warps on every sub-partition busy,
+      // each of the few scalar instructions between two tiles costs cycles
+      // that no other work hides)
+      const float cq = p.scale_log2 * qd;
+      const float lvref = ptx::lg2(vref);
       auto fp8_factors = [&](float kd, float vd, float& cjo, float& bo, float& sso) {
-        const float rj = vd / vref;   // in (0, 1]
-        cjo = p.scale_log2 * qd * kd;
-        bo = C::PSHIFT + ptx::lg2(rj);
-        sso = 1.f / rj;
+        const float lr = ptx::lg2(vd) - lvref;   // log2 of V block scale / largest, <= 0
+        cjo = cq * kd;
+        bo = C::PSHIFT + lr;
+        sso = ptx::ex2(-lr);
       };
       if constexpr (DT == DT_E4M3) {
         fp8_factors(__ldg(kd_row + U.j0), __ldg(vd_row + U.j0), cj_cur, bias_cur, ssc_cur);
@@ -692,6 +861,12 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         float rmax;
         if (!masked) ptx::tmem_ld_max_x128(tS, sr, rmax);
         else ptx::tmem_ld_x128(tS, sr);
+        if constexpr (C::PSMEM) {
+          // S_s is in registers: the next S GEMM of this tile may overwrite it
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(B_SFREE + s));
+        }
         float sv[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
@@ -734,6 +909,20 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
           li *= alpha;
           rescale = true;
         }
+        if constexpr (C::PSMEM) {
+          // the P buffer is free, and O_s holds the previous PV product, once
+          // the previous PV GEMM of this tile is done
+          // buffer p_cnt % 2 is free once PV number p_cnt - 2 is done; O_s holds
+          // every previous PV product (needed before a rescale) once PV
+          // number p_cnt - 1 is done
+          const bool any_rescale = __any_sync(0xffffffffu, rescale);
+          const int wait_n = any_rescale ? p_cnt - 1 : p_cnt - 2;
+          if (wait_n >= 0) {
+            ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (wait_n & 1)), (wait_n >> 1) & 1, ctl);
+            if (!ok) break;
+            ptx::tc_fence_after();
+          }
+        }
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
           for (int cb = 0; cb < D; cb += 32) {
@@ -749,6 +938,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         // chunks as they are produced (the whole S row is already in registers)
         const float nbias = bias_extra - mi;
         float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+        const uint32_t prow = prow0 + (uint32_t)(p_cnt & 1) * C::PBYTES;   // shared-memory P
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -770,7 +960,14 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
               const int e = 32 * k + 4 * c;
               pk[c] = ptx::pack_e4m3x4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
             }
-            ptx::tmem_st_x8(tS + 8 * k, pk);
+            if constexpr (C::PSMEM) {
+              // keys 32k .. 32k+31 are the 16-byte chunks 2k, 2k+1 of the row
+              // (K-major, 128-byte swizzle: chunk c of row r sits at c ^ (r % 8))
+              ptx::st_shared_v4(prow + (((2 * k) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+              ptx::st_shared_v4(prow + (((2 * k + 1) ^ (r & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+            } else {
+              ptx::tmem_st_x8(tS + 8 * k, pk);
+            }
           } else {
             uint32_t pk[16];
 #pragma unroll
@@ -785,8 +982,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         li += ((sum0 + sum1) + (sum2 + sum3)) * sum_scale;
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
+        if constexpr (C::PSMEM) ptx::fence_proxy_async_smem();   // P visible to the MMA
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(B_PFULL + s));
+        if (lane == 0) ptx::mbar_arrive(bar(C::PSMEM ? B_PFULLB + 2 * s + (p_cnt & 1) : B_PFULL + s));
+        ++p_cnt;
         if constexpr (DT == DT_E4M3) {
           if (j + 1 < ns) {
             fp8_factors(kd_next, vd_next, cj_cur, bias_cur, ssc_cur);

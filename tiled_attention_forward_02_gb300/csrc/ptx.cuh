@@ -106,6 +106,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// 16-byte shared-memory store
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// this thread's shared-memory writes become visible to the async proxy
+// (tensor core operands read from shared memory)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------ tensor memory
 // allocate `ncols` (power of two >= 32) columns; the base address is written
 // to shared memory at `dst`.  Whole warp, convergent.
