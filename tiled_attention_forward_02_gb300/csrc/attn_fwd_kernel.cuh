@@ -18,7 +18,9 @@
 //   * MMA warp: one thread issues tcgen05.mma S_s = Q_s K_j^T into tensor
 //     memory and O_s += P_s V_j with P_s read from tensor memory; stage order
 //     PV_0(j-1), S_0(j), PV_1(j-1), S_1(j) makes one tile's softmax overlap
-//     the other tile's two GEMMs (the pages' ping-pong);
+//     the other tile's two GEMMs (the pages' ping-pong). That thread shares
+//     its sub-partition with two softmax warps and waits for a scheduler slot
+//     on every instruction, so its steady-state loop is kept short;
 //   * softmax warpgroups (one per query tile, one thread per query row =
 //     one TMEM lane): tcgen05.ld of the S row, mask, row max, conditional
 //     rescale of O in tensor memory, exp2, row sum, P rounded to the input
@@ -29,8 +31,11 @@
 // construction, and mbarriers + tcgen05.commit replace the named barriers.
 //
 // Tensor memory (512 columns x 128 lanes, FP32): S_s at column 128 s,
-// O_s at 128 QST + D s.  P_s (16-bit: 64 columns, 8-bit: 32 columns) is
-// written over the first columns of S_s after S_s has been read.
+// O_s at 128 QST + D s.  16-bit P_s (64 columns) is written over the first
+// columns of S_s after S_s has been read. FP8 with two query tiles writes P_s
+// to one of two shared-memory buffers of its tile instead and releases S_s as
+// soon as it is in registers, so the tile's next S GEMM runs while its softmax
+// still computes P (order per key tile: S_0(j), PV_0(j-1), S_1(j), PV_1(j-1)).
 //
 // FP8 (E4M3) instance: per-128-token-block descales are applied to the
 // logits per 128 x 128 tile; P is quantised to E4M3 with the V block's scale
@@ -149,9 +154,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
-}
-__device__ __forceinline__ uint64_t sdesc_of(uint32_t lo) {
-  return ((uint64_t)kSdescHi << 32) | lo;
 }
 
 // S = Q K^T: one MMA per 32 bytes of the head dimension; the operands' low

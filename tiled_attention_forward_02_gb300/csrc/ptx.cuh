@@ -172,32 +172,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// the same MMAs with the accumulate flag as an immediate (no predicate
-// set-up per MMA on the issuing thread): ACC = 0 overwrites D, 1 adds to it
-template <int ACC>
-__device__ __forceinline__ void mma_f16_ss_c(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, %4;" ::"r"(d), "l"(a), "l"(b),
-               "r"(idesc), "n"(ACC)
-               : "memory");
-}
-template <int ACC>
-__device__ __forceinline__ void mma_f16_ts_c(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, %4;" ::"r"(d), "r"(a_tmem),
-               "l"(b), "r"(idesc), "n"(ACC)
-               : "memory");
-}
-template <int ACC>
-__device__ __forceinline__ void mma_f8_ss_c(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, %4;" ::"r"(d), "l"(a),
-               "l"(b), "r"(idesc), "n"(ACC)
-               : "memory");
-}
-template <int ACC>
-__device__ __forceinline__ void mma_f8_ts_c(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
-  asm volatile("tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, %4;" ::"r"(d), "r"(a_tmem),
-               "l"(b), "r"(idesc), "n"(ACC)
-               : "memory");
-}
 // The same two MMA forms with each shared-memory descriptor built inside the
 // instruction's own asm block from a low word (register) plus an offset and
 // the high word (immediates): the issuing thread holds one register per
