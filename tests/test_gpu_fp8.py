@@ -127,6 +127,27 @@ def test_fp8_forward_vs_dequantised_oracle(gpu_lib, causal, hadamard, d):
     assert e["lse_max_abs"] <= (1e-2 if hadamard else 2e-3), e
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_several_units_per_cta(gpu_lib, causal):
+    """GQA with several work units per persistent CTA (B=1, Hq=32, Hkv=4,
+    N=4096: 512 units of 256 query rows), so that the per-tile barrier phases
+    (S released, P buffers full and free) carry over unit boundaries; sampled
+    rows of every head against the oracle on the dequantised inputs."""
+    B, N, Hq, Hkv, d = 1, 4096, 32, 4, 128
+    q, k, v = synth.attn_inputs(B, N, N, Hq, Hkv, d, dtype=torch.bfloat16, seed=31,
+                                outlier_frac=1e-3, outlier_scale=10.0, device="cuda")
+    o, lse = _fp8_forward(gpu_lib, q, k, v, causal, False, Hkv)
+    rows = synth.sample_rows(B, Hq, N, per_head=16, seed=3)
+    idx = torch.as_tensor(rows, device="cuda")
+    og = o[idx[:, 0], idx[:, 2], idx[:, 1]].double().cpu().numpy()
+    lg = lse[idx[:, 0], idx[:, 1], idx[:, 2]].double().cpu().numpy()
+    o_ref, lse_ref = _oracle_dequant(q, k, v, causal, False, Hkv, rows=rows)
+    assert np.isfinite(og).all() and np.isfinite(lg).all()
+    rel_rms = math.sqrt(np.mean((og - o_ref) ** 2) / np.mean(o_ref ** 2))
+    assert rel_rms <= 4e-2, rel_rms
+    assert np.max(np.abs(lg - lse_ref)) <= 2e-3, np.max(np.abs(lg - lse_ref))
+
+
 @pytest.mark.parametrize("outlier_scale", [50.0, 10.0])
 def test_fp8_full_workload_accuracy_and_hadamard(gpu_lib, outlier_scale):
     """B=4, H=16, N=4096, d=128, 0.1% of entries multiplied by `outlier_scale`.
