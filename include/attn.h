@@ -299,6 +299,18 @@ const char* attn_strerror(int code);
  * process so far (monotonic; used to count launches in a timed region). */
 int64_t attn_launch_count(void);
 
+/*
+ * attn_selftest_bounded_wait - exercises the failure path of the kernels'
+ * waits: launches one warp on `stream` that waits, with the same bounded wait
+ * every kernel of the library uses, on an mbarrier that nothing arrives on.
+ * The wait gives up after its budget (about 2 s of GPU clock), sets the
+ * timeout bit of the device status word and the kernel returns; the next
+ * attn_get_status reports ATTN_ERR_TIMEOUT and clears the word.  No fault,
+ * trap or hang is involved and the context stays usable.  For tests.
+ *   Returns ATTN_OK once launched, ATTN_ERR_CUDA if the launch failed.
+ */
+int attn_selftest_bounded_wait(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

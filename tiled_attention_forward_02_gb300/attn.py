@@ -26,7 +26,7 @@ ERR_SCRATCH = -7
 EXPORTS = ("attn_fwd", "attn_prep_fp8", "attn_fwd_fp8", "attn_get_status", "attn_strerror",
            "attn_launch_count", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_prep_fp8_per_tensor",
-           "attn_rope_table", "attn_prep_fp8_rope")
+           "attn_rope_table", "attn_prep_fp8_rope", "attn_selftest_bounded_wait")
 
 _lib = None
 
@@ -56,6 +56,8 @@ def load():
                                  f32, i32, vp]
     lib.attn_get_status.restype = i32
     lib.attn_get_status.argtypes = [vp]
+    lib.attn_selftest_bounded_wait.restype = i32
+    lib.attn_selftest_bounded_wait.argtypes = [vp]
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_strerror.argtypes = [i32]
     lib.attn_launch_count.restype = i64
@@ -306,3 +308,9 @@ def attn_fwd_fp8(q8, k8, v8t, q_descale, k_descale, v_descale, *, Hq: int | None
 def get_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word as a code."""
     return int(load().attn_get_status(_stream(stream)))
+
+
+def selftest_bounded_wait(stream=None):
+    """Launch the library's bounded-wait self test (a wait that runs out after
+    about 2 s and sets the timeout status); read the result with get_status."""
+    _check(int(load().attn_selftest_bounded_wait(_stream(stream))), "attn_selftest_bounded_wait")

@@ -472,3 +472,32 @@ extern "C" const char* attn_strerror(int code) {
 }
 
 extern "C" int64_t attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+namespace attn {
+namespace {
+// one warp waits, with the kernels' own bounded wait, on an mbarrier whose
+// phase never completes: the wait gives up after its budget, sets the abort
+// flag and the timeout bit of the status word, and the kernel returns
+__global__ void bounded_wait_selftest_kernel(unsigned int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_addr(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  const Ctl ctl{&abort_flag, status};
+  warp_wait_bar(ptx::smem_addr(&bar), 0, ctl);
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_selftest_bounded_wait(void* stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != ATTN_OK) return rc;
+  attn::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status);
+  note_launch();
+  return check_launch();
+}
