@@ -692,6 +692,51 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
               if (!ok) break;
             }
           }
+          if constexpr (QST == 1 && !SPLIT) {
+            // the same steady state with one query tile: PV(j-1), S(j)
+            const int jend = U.n_s[0] - 1;
+            if (j == 2 && jend > 2) {
+              int vs = (kv_it + 3) % NSLOT;
+              uint32_t vph = ((kv_it + 3) / NSLOT) & 1;
+              int ks = (kv_it + 4) % NSLOT;
+              uint32_t kph = ((kv_it + 4) / NSLOT) & 1;
+              uint32_t pph = pv_cnt[0] & 1;
+              const uint32_t qlo0 = sdesc_lo(sQ, 16);
+              const uint32_t tS0 = tmem + C::S_COL0, tO0 = tmem + C::O_COL0;
+              bool sok = true;
+              for (; j < jend; ++j) {
+                const uint32_t vlo = sdesc_lo(sKV + vs * C::KVBYTES, DT == DT_E4M3 ? 16 : C::CHUNK_BYTES);
+                const uint32_t klo = sdesc_lo(sKV + ks * C::KVBYTES, 16);
+                sok &= wait_bar(bar(B_KVFULL + vs), vph, ctl);
+                sok &= wait_bar(bar(B_PFULL + 0), pph, ctl);
+                ptx::tc_fence_after();
+                issue_pv(tO0, tS0, vlo);
+                ptx::tc_commit(bar(B_KVEMPTY + vs));
+                sok &= wait_bar(bar(B_KVFULL + ks), kph, ctl);
+                ptx::tc_fence_after();
+                issue_s(tS0, qlo0, klo);
+                ptx::tc_commit(bar(B_SFULL + 0));
+                ptx::tc_commit(bar(B_KVEMPTY + ks));
+                pph ^= 1u;
+                vs = ks + 1;
+                vph = kph;
+                if (vs == NSLOT) {
+                  vs = 0;
+                  vph ^= 1u;
+                }
+                ks = vs + 1;
+                kph = vph;
+                if (ks == NSLOT) {
+                  ks = 0;
+                  kph ^= 1u;
+                }
+                if (!sok) break;
+              }
+              pv_cnt[0] += j - 2;
+              ok = sok;
+              if (!ok) break;
+            }
+          }
           const int k_idx = kv_it + 2 * j;       // ring index of K_j
           const int v_idx = kv_it + 2 * j - 1;   // ring index of V_{j-1}
           const int kslot = k_idx % NSLOT;
