@@ -20,9 +20,10 @@
 // shuffles across the LPR lanes of the row), scaled by 1/sqrt(d); the
 // block amax is reduced through shared memory; codes are y * (448 / amax)
 // (float32, the reciprocal rounded once per block) rounded to nearest-even and
-// saturated to +-448 by the hardware conversion; descale = amax / 448.  The
-// kernel is bandwidth-bound: it reads each bf16 element once and writes one
-// byte per element.
+// saturated to +-448 by the hardware conversion; descale = amax / 448.  It
+// reads each bf16 element once and writes one byte per element, an HBM-bound
+// amount of work; at two CTAs of 8 warps per SM (register and shared-memory
+// limits) the kernel itself is bound by instruction latency, not bandwidth.
 //
 // Two variants share the kernel:
 // * rotary embedding before the transform (the summary card notes that the
