@@ -9,11 +9,12 @@ Sources and readings
   brought back to its floating-point range; dequantisation is fused into the
   attention pipeline.  Reading taken: symmetric per-block scale, no offset
   (FP8 is sign-magnitude), one block = 128 tokens x d of one (batch, head);
-  descale = amax / 448 (448 = largest finite E4M3 value), descale = 1 for an
-  all-zero block; code = E4M3(x * (448 / amax)) rounded to nearest-even with
-  saturation to +-448 (the reciprocal 448 / amax is rounded to float32 once
-  per block, as is the product).  The last block of a sequence may be
-  partial.
+  descale = amax / 448 (448 = largest finite E4M3 value) rounded to float32,
+  descale = 1 for an all-zero block; code = E4M3(x / descale) rounded to
+  nearest-even with saturation to +-448, the quotient of the float32 value
+  and the float32 descale taken exactly (no intermediate rounding that could
+  move it across an E4M3 rounding boundary).  The last block of a sequence
+  may be partial.
 * FP8 format: the pages say "FP8" (H100 FP8 tensor cores, 1978 TFLOPS, in
   the Together AI summary card "FlashAttention-3——利用异步与低精度加速注意力机制");
   the code on the dtcms.com page (section 11, FP8Support.fp32_to_fp8_conversion)
@@ -34,7 +35,7 @@ Sources and readings
   same section, says incoherent processing gives 2.6 times lower error than
   "baseline FP8" without naming that baseline.  Reading taken: one scale for
   the whole tensor (all batches, heads and tokens), descale = amax / 448,
-  codes and the float32 reciprocal and product as for a block.  The descale
+  codes = E4M3(x / descale) as for a block.  The descale
   is written for every (b, head, block) so that the same forward consumes
   either scheme.
 * Rotary embedding fused with the transform: the summary card, same section,
@@ -47,12 +48,16 @@ Sources and readings
   transform (the rotation must act on the model's own Q and K; M is applied
   after it so that Q M (K M)^T is still the rotated Q K^T), never to V.
 
-Precision of the quantisation decision: the block amax, the descale
-amax / 448, the reciprocal 448 / amax and the product x * (448 / amax) are
-taken in float32 with IEEE round-to-nearest, as the kernel does, so that codes
-can be compared bit for bit where the transformed values are themselves exact
-in float32 (no Hadamard).  With the Hadamard transform the oracle forms the product in
-float64 and rounds once to float32.
+Precision of the quantisation decision: the values that are quantised are
+float32 (the inputs themselves, or the rotated / transformed values formed in
+float64 and rounded once to float32); the block amax is exact; the descale
+amax / 448 is rounded to float32 once (it is what the forward pass reads); the
+code is the E4M3 rounding of the exact quotient value / descale.  The
+quotient is formed in float64: a float32 value over a float32 descale lies
+on an E4M3 rounding midpoint exactly when its float64 rounding does (a
+midpoint times the descale has at most 29 significant bits, so a quotient
+that misses a midpoint misses it by far more than a float64 ulp), so the
+float64 division decides every code as the exact quotient would.
 """
 from __future__ import annotations
 
@@ -150,10 +155,9 @@ def quantize_blocks(y32: np.ndarray, block: int = BLOCK):
         blk = y32[:, n0:n1]                                   # [B, n, H, d]
         amax = np.abs(blk).max(axis=(1, 3)).astype(np.float32)  # [B, H], exact
         ds = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-        inv = np.where(amax > 0, np.float32(E4M3_MAX) / np.where(amax > 0, amax, np.float32(1.0)),
-                       np.float32(1.0)).astype(np.float32)
         descale[:, :, t] = ds
-        q = (blk * inv[:, None, :, None]).astype(np.float32)  # IEEE float32 product
+        # q = x / descale, decided as the exact quotient (see the module notes)
+        q = blk.astype(np.float64) / ds.astype(np.float64)[:, None, :, None]
         codes[:, n0:n1] = e4m3_encode(q)
     return codes, descale
 
@@ -168,12 +172,8 @@ def quantize_tensor(y32: np.ndarray, block: int = BLOCK):
     B, N, H, d = y32.shape
     nb = (N + block - 1) // block
     amax = np.float32(np.abs(y32).max()) if y32.size else np.float32(0.0)
-    if amax > 0:
-        ds = np.float32(amax / np.float32(E4M3_MAX))
-        inv = np.float32(np.float32(E4M3_MAX) / amax)
-    else:
-        ds = inv = np.float32(1.0)
-    codes = e4m3_encode((y32 * inv).astype(np.float32))   # IEEE float32 product
+    ds = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+    codes = e4m3_encode(y32.astype(np.float64) / np.float64(ds))   # exact quotient decides
     return codes, np.full((B, H, nb), ds, dtype=np.float32)
 
 

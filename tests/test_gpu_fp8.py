@@ -2,9 +2,13 @@
 optional Hadamard transform; the per-tensor baseline; the fused rotary
 variant and its tables) and the FP8 fused forward.
 
-* Prep without the transform: the quantised values are exact float32
-  quotients on both sides, so codes and descales must match the oracle bit
-  for bit (BSHD and transposed layouts).
+* Prep without the transform: descales must match the oracle bit for bit.
+  The oracle's code is E4M3(x / descale) of the exact quotient; the kernel
+  scales by the float32 reciprocal 448 / amax (a documented speed choice, a
+  relative difference below 2^-21), so a code may differ from the oracle's
+  only where that difference straddles an E4M3 rounding midpoint: every code
+  must be one of the two codes of the quotient's 2^-21 neighbourhood, and the
+  codes that differ from the oracle's are counted and bounded.
 * Prep with the transform: the float32 butterfly and the oracle's float64
   product may round the last bit differently, which can move a value across
   an E4M3 rounding boundary.  Codes are checked against the exact value with
@@ -42,15 +46,37 @@ def test_prep_bit_exact_without_transform(gpu_lib, d, N):
     codes, ds = gpu_lib.attn_prep_fp8(x.cuda())
     codes_t, ds_t = gpu_lib.attn_prep_fp8(x.cuda(), transpose_out=True)
     assert gpu_lib.get_status() == 0
-    oc, ods, _ = ofp8.prepare(x.float().numpy(), None, False)
+    xf = x.float().numpy()
+    oc, ods, _ = ofp8.prepare(xf, None, False)
     np.testing.assert_array_equal(ds.cpu().numpy(), ods)
     np.testing.assert_array_equal(ds_t.cpu().numpy(), ods)
-    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
+    t = np.arange(N) // 128
+    q_exact = xf.astype(np.float64) / ods.astype(np.float64)[:, :, t].transpose(0, 2, 1)[..., None]
+    g = codes.cpu().numpy()
+    n_diff = _codes_at_midpoints_only(g, oc, q_exact)
     npad = (N + 15) // 16 * 16
     ct = codes_t.cpu().numpy()
     assert ct.shape == (B, H, d, npad)
-    np.testing.assert_array_equal(ct[..., :N], oc.transpose(0, 2, 3, 1))
+    # both layouts carry the same codes
+    np.testing.assert_array_equal(ct[..., :N], g.transpose(0, 2, 3, 1))
     assert not ct[..., N:].any()   # padding keys are zero codes
+    print(f"codes off the oracle's at a rounding midpoint: {n_diff} of {g.size}")
+
+
+def _codes_at_midpoints_only(g, oc, q_exact, rel=2.0 ** -21, max_frac=1e-3):
+    """g (GPU codes) equals oc (oracle codes, E4M3 of the exact quotient)
+    except where the exact quotient lies within `rel` of an E4M3 rounding
+    midpoint; there g must be the code of the other side.  Returns how many
+    codes differ (bounded by max_frac of all codes)."""
+    lo = ofp8.e4m3_encode(q_exact * (1 - rel * np.sign(q_exact)))
+    hi = ofp8.e4m3_encode(q_exact * (1 + rel * np.sign(q_exact)))
+    ok = (g == oc) | (g == lo) | (g == hi)
+    assert ok.all(), np.argwhere(~ok)[:5]
+    n_diff = int(np.count_nonzero(g != oc))
+    # a code that differs is one whose neighbourhood holds a midpoint
+    assert np.all(lo[g != oc] != hi[g != oc])
+    assert n_diff <= max_frac * g.size, n_diff
+    return n_diff
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
@@ -66,7 +92,7 @@ def test_prep_with_transform_matches_oracle(gpu_lib, d):
     g_ds = ds.cpu().numpy()
     np.testing.assert_allclose(g_ds, ods, rtol=4e-6, atol=0)
     t = np.arange(N) // 128
-    q_exact = y64 / g_ds.astype(np.float64)[:, :, t].transpose(0, 2, 1)[..., None]
+    q_exact = y64 / ods.astype(np.float64)[:, :, t].transpose(0, 2, 1)[..., None]
     tol = 4e-6 * np.abs(q_exact) + 1e-30
     lo, hi = ofp8.e4m3_encode(q_exact - tol), ofp8.e4m3_encode(q_exact + tol)
     g = codes.cpu().numpy()
@@ -195,11 +221,13 @@ def test_prep_per_tensor_bit_exact_without_transform(gpu_lib, d):
     codes, ds = gpu_lib.attn_prep_fp8_per_tensor(x.cuda())
     codes_t, ds_t = gpu_lib.attn_prep_fp8_per_tensor(x.cuda(), transpose_out=True)
     assert gpu_lib.get_status() == 0
-    oc, ods, _ = ofp8.prepare(x.float().numpy(), per_tensor=True)
+    xf = x.float().numpy()
+    oc, ods, _ = ofp8.prepare(xf, per_tensor=True)
     np.testing.assert_array_equal(ds.cpu().numpy(), ods)
     np.testing.assert_array_equal(ds_t.cpu().numpy(), ods)
-    np.testing.assert_array_equal(codes.cpu().numpy(), oc)
-    np.testing.assert_array_equal(codes_t.cpu().numpy()[..., :N], oc.transpose(0, 2, 3, 1))
+    g = codes.cpu().numpy()
+    _codes_at_midpoints_only(g, oc, xf.astype(np.float64) / np.float64(ods.flat[0]))
+    np.testing.assert_array_equal(codes_t.cpu().numpy()[..., :N], g.transpose(0, 2, 3, 1))
     # a second call on other data leaves nothing behind (descale[0] is reused
     # as the amax accumulator)
     z = torch.zeros_like(x).cuda()
@@ -229,7 +257,7 @@ def test_prep_per_tensor_with_transform(gpu_lib):
     g_ds = ds.cpu().numpy()
     np.testing.assert_allclose(g_ds, ods, rtol=4e-6, atol=0)
     assert np.all(g_ds == g_ds.flat[0])
-    _codes_near(codes.cpu().numpy(), y64 / float(g_ds.flat[0]))
+    _codes_near(codes.cpu().numpy(), y64 / float(ods.flat[0]))
 
 
 # --- rotary embedding fused into the prep -------------------------------------
@@ -270,7 +298,7 @@ def test_prep_rope_matches_oracle(gpu_lib, d, hadamard):
     g_ds = ds.cpu().numpy()
     np.testing.assert_allclose(g_ds, ods, rtol=4e-6, atol=0)
     t = np.arange(N) // 128
-    q_exact = y64 / g_ds.astype(np.float64)[:, :, t].transpose(0, 2, 1)[..., None]
+    q_exact = y64 / ods.astype(np.float64)[:, :, t].transpose(0, 2, 1)[..., None]
     _codes_near(codes.cpu().numpy(), q_exact)
 
 
@@ -329,6 +357,6 @@ def test_prep_rope_hadamard_full_size_sampled(gpu_lib):
     rot = np.concatenate([a * c - b * s_, b * c + a * s_], axis=-1)
     sg = signs.cpu().numpy().astype(np.float64)[rows[:, 1]]
     y = (rot * sg) @ ofp8.hadamard_matrix(d).astype(np.float64) / np.sqrt(d)
-    q_exact = y / g_ds.astype(np.float64)[rows[:, 0], rows[:, 1], rows[:, 2] // 128][:, None]
+    q_exact = y / ods.astype(np.float64)[rows[:, 0], rows[:, 1], rows[:, 2] // 128][:, None]
     g = codes.cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
     _codes_near(g, q_exact)

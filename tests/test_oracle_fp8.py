@@ -98,10 +98,56 @@ def test_block_quantisation_properties():
                 dec = fp8.e4m3_decode(codes[b, t * 128:(t + 1) * 128, h])
                 # spacing of E4M3 at |q|: 2^(floor(log2|q|) - 3), at least 2^-9
                 e = np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6)))
-                # (the scaled value is x * fl(448 / amax), within 2^-23 relative of
-                # x / descale, so a value on a rounding midpoint may round either way)
-                assert np.all(np.abs(dec - q) <= 0.5 * np.exp2(e - 3) * (1 + 1e-5))
+                assert np.all(np.abs(dec - q) <= 0.5 * np.exp2(e - 3) * (1 + 1e-6))
                 assert np.abs(dec).max() == 448.0
+                np.testing.assert_array_equal(codes[b, t * 128:(t + 1) * 128, h].ravel(),
+                                              _nearest_code(q))
+
+
+def _nearest_code(q):
+    """Brute force over the E4M3 codebook, independent of fp8.e4m3_encode:
+    the finite code whose value (from its bit fields) is nearest to q, ties to
+    the code with the even last significand bit, beyond +-448 the largest
+    finite magnitude."""
+    q = np.asarray(q, dtype=np.float64).ravel()
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.int64)
+    e, m = (codes >> 3) & 0xF, codes & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (8 + m) * 2.0 ** (e - 10))
+    val = np.where(codes & 0x80, -mag, mag)
+    dist = np.abs(q[:, None] - val[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    tie = dist == best
+    # among tied codes take the even significand (one of two neighbours is
+    # even); +0 and -0 tie for 0: prefer the sign of q
+    score = np.where(tie, 0, 4) + (codes[None, :] & 1) * 2 + (
+        (codes[None, :] >> 7) != (np.signbit(q)[:, None]).astype(np.int64))
+    return codes[np.argmin(score, axis=1)].astype(np.uint8)
+
+
+def test_block_quantisation_rounds_exact_quotient_at_midpoints():
+    """Values placed exactly on E4M3 rounding midpoints of x / descale round
+    to the even neighbour, and values one float32 ulp off a midpoint round
+    to the nearer side: the code is decided by the exact quotient x / descale
+    ("FlashAttention（V3）深度解析" section 4.3: a scale per block; the
+    quantised value is the block's value divided by its scale)."""
+    # block amax 448 * 2^-4 = 28: descale = 1/16 exactly, so x / descale = 16 x
+    mids = np.array([1.0625, 1.1875, 3.125, 13.5, 200.0, 2.0 ** -10, 3 * 2.0 ** -10], np.float64)
+    x = (mids / 16.0).astype(np.float32)
+    assert np.array_equal(x.astype(np.float64) * 16.0, mids)      # exactly on midpoints
+    up = np.nextafter(x, np.float32(np.inf))
+    dn = np.nextafter(x, np.float32(0.0))
+    blk = np.zeros((1, 128, 1, 4), np.float32)
+    blk[0, 0, 0, 0] = 28.0
+    vals = np.concatenate([x, up, dn])
+    blk[0, 1:1 + len(vals), 0, 0] = vals
+    codes, ds = fp8.quantize_blocks(blk)
+    assert ds[0, 0, 0] == np.float32(1.0 / 16.0)
+    got = codes[0, 1:1 + len(vals), 0, 0]
+    np.testing.assert_array_equal(got, _nearest_code(vals.astype(np.float64) * 16.0))
+    dec = fp8.e4m3_decode(got).reshape(3, -1)
+    assert np.all(dec[1] > dec[2])          # one ulp above / below a midpoint split
+    # ties to even: 1.0625 -> 1.0 (code 0x38), 1.1875 -> 1.25 (0x3A)
+    assert got[0] == 0x38 and got[1] == 0x3A
 
 
 def test_fp8_error_with_hadamard_not_worse_on_outliers():
@@ -205,11 +251,11 @@ def test_per_tensor_quantisation_properties():
     assert np.all(ds == np.float32(amax / np.float32(448.0)))
     dec = fp8.e4m3_decode(codes)
     assert np.abs(dec).max() == 448.0
-    # every value is within half a quantum of its scaled value (a midpoint
-    # may round either way: the scale is x * fl(448 / amax))
-    qv = y.astype(np.float64) * (448.0 / float(amax))
+    # every code is the E4M3 rounding of value / descale
+    qv = y.astype(np.float64) / np.float64(ds.flat[0])
     e = np.floor(np.log2(np.maximum(np.abs(qv), 2.0 ** -6)))
-    assert np.all(np.abs(dec - qv) <= 0.5 * np.exp2(e - 3) * (1 + 1e-5))
+    assert np.all(np.abs(dec - qv) <= 0.5 * np.exp2(e - 3) * (1 + 1e-6))
+    np.testing.assert_array_equal(codes[:, :, :, :8].ravel(), _nearest_code(qv[:, :, :, :8]))
     # a tensor of one block is quantised as that block
     one = y[:1, :128, :1]
     c1, d1, _ = fp8.prepare(one, per_tensor=True)
