@@ -491,6 +491,100 @@ class E2EPipeline:
         return start.elapsed_time(end)
 
 
+def timed_region(step, steps, warmup, world, rank, local):
+    """W untimed warm-up steps, then `steps` timed steps bracketed by a
+    barrier and a synchronize on both sides, with CUDA events on the
+    launching stream around every launch of the dominant kernel and around
+    the whole region, and nvidia-smi clocks sampled meanwhile.
+    Returns (per-launch ms list, total ms, clocks summary, launches)."""
+    import torch
+
+    from tiled_attention_forward_02_gb300 import attn
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if attn.get_status() != 0:
+        raise RuntimeError("device status reported an error during warm-up")
+    sampler = ClockSampler(local if world > 1 else torch.cuda.current_device())
+    if rank == 0 or world > 1:
+        sampler.start()
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = attn.launch_count()
+    t_wall0 = time.time()
+    t_start.record(stream)
+    for i in range(steps):
+        step(kev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    launches = attn.launch_count() - n0
+    per_launch_ms = [a.elapsed_time(b) for a, b in kev]
+    total_ms = t_start.elapsed_time(t_end)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    sampler.stop()
+    return per_launch_ms, total_ms, clocks, launches
+
+
+def tensor_roofline(wl, meta, per_launch_ms, peaks, peak_src):
+    """Roofline of the dominant (tensor-core) kernel: algorithmic FLOPs per
+    launch over its mean CUDA-event launch time, against the measured dense
+    peak of its input type."""
+    avg = sum(per_launch_ms) / len(per_launch_ms)
+    achieved = meta["flops"] / (avg * 1e-3) / 1e12
+    if WORKLOADS[wl][7] == "bf16":
+        peak, note = peaks["bf16_tflops"], f"dense bf16, {peak_src} burst"
+    else:
+        peak = 2.0 * peaks["bf16_tflops"]
+        note = f"dense fp8 = 2 x {peak_src} bf16 burst (nominal fp8:bf16 ratio)"
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": note, "kernel": meta["kernel"],
+            "traffic": recorded_traffic(meta["kernel"], wl)}
+
+
+def prep_roofline(meta, peaks):
+    if not meta.get("prep_events"):
+        return None
+    pms = [a.elapsed_time(b) for a, b in meta["prep_events"]]
+    pms = sum(pms) / len(pms)
+    gbs = meta["prep_bytes"] / (pms * 1e-3) / 1e9
+    return {"kernel": "prep_fp8_kernel (Q, K, V)", "ms_per_step": pms, "bound": "hbm",
+            "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": meta["prep_bytes"]}
+
+
+def fp8_record(wl, args, world, rank, local, dev, peaks, peak_src):
+    """The FP8 workload measured in the same run as the headline line: one
+    step = the prep of Q, K, V plus the FP8 forward, timed like the main
+    workload (device-resident inputs); kernel-alone times of the forward and
+    of the three prep launches from CUDA events on their stream."""
+    import torch
+    step, _, meta = make_step(wl, dev)
+    per_launch_ms, total_ms, clocks, launches = timed_region(step, args.steps, args.warmup,
+                                                             world, rank, local)
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+    rec = {
+        "workload": wl, "value": world * meta["flops"] / (ms_step * 1e-3) / 1e12,
+        "unit": "TFLOPS", "ms_per_step": ms_step, "steps": args.steps, "warmup": args.warmup,
+        "dtype": "e4m3", "config": config_of(wl),
+        "roofline": tensor_roofline(wl, meta, per_launch_ms, peaks, peak_src),
+        "prep_roofline": prep_roofline(meta, peaks),
+        "kernel_ms": {"avg": sum(per_launch_ms) / len(per_launch_ms),
+                      "median": statistics.median(per_launch_ms),
+                      "min": min(per_launch_ms), "max": max(per_launch_ms)},
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "gpu_launches": launches,
+    }
+    del step, meta
+    torch.cuda.empty_cache()
+    return rec
+
+
 def gpu_arm(args, rank, world, local):
     import torch
 
@@ -502,37 +596,9 @@ def gpu_arm(args, rank, world, local):
     stream = torch.cuda.current_stream()
     flops = meta["flops"]
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if attn.get_status() != 0:
-        raise RuntimeError("device status reported an error during warm-up")
-
-    sampler = ClockSampler(local if world > 1 else torch.cuda.current_device())
-    if rank == 0 or world > 1:
-        sampler.start()
     # ---- timed region: device-resident inputs
-    # events around every launch of the dominant kernel, on its stream, plus
-    # one pair around the whole timed region
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    n0 = attn.launch_count()
-    t_wall0 = time.time()
-    t_start.record(stream)
-    for i in range(args.steps):
-        step(kev[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier(world)
-    launches = attn.launch_count() - n0
-    per_launch_ms = [a.elapsed_time(b) for a, b in kev]
-    total_ms = t_start.elapsed_time(t_end)
-    clocks = sampler.summary(t_wall0, t_wall1)
-    sampler.stop()
+    per_launch_ms, total_ms, clocks, launches = timed_region(step, args.steps, args.warmup,
+                                                             world, rank, local)
     status = attn.get_status()
 
     ms_step = max_over_ranks(total_ms / args.steps, world)
@@ -547,9 +613,16 @@ def gpu_arm(args, rank, world, local):
     e2e_ms = max_over_ranks(pipe.run(e2e_steps) / e2e_steps, world)
     barrier(world)
 
+    peaks, peak_src = load_peaks()
+    # the FP8 workload (B4 H16 N4096 d128, x50 outliers), plain and with the
+    # transform, measured in the same run beside the headline workload
+    fp8 = None
+    if wl == DEFAULT_WORKLOAD and not args.no_fp8:
+        fp8 = [fp8_record(w, args, world, rank, local, dev, peaks, peak_src)
+               for w in ("fp8_e4m3_B4_H16_N4096_d128", "fp8_e4m3_hadamard_B4_H16_N4096_d128")]
+
     if rank != 0:
         return
-    peaks, peak_src = load_peaks()
     avg_launch_ms = sum(per_launch_ms) / len(per_launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12   # dominant kernel alone
     kind = WORKLOADS[wl][7]
@@ -580,14 +653,7 @@ def gpu_arm(args, rank, world, local):
         "peak": exp_peak / 1e9, "unit": "Gexp/s",
         "frac": exps / (avg_launch_ms * 1e-3) / exp_peak,
         "peak_source": "SMs x 32 exp2 per cycle x median SM clock"}
-    prep = None
-    if meta.get("prep_events"):
-        pms = [a.elapsed_time(b) for a, b in meta["prep_events"]]
-        pms = sum(pms) / len(pms)
-        gbs = meta["prep_bytes"] / (pms * 1e-3) / 1e9
-        prep = {"kernel": "prep_fp8_kernel (Q, K, V)", "ms_per_step": pms, "bound": "hbm",
-                "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": meta["prep_bytes"]}
+    prep = prep_roofline(meta, peaks)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -614,6 +680,8 @@ def gpu_arm(args, rank, world, local):
         "status": status,
         "kernel_source_hash": kernel_source_hash(),
     }
+    if fp8 is not None:
+        line["fp8"] = fp8
     print(json.dumps(line), flush=True)
 
 
@@ -625,6 +693,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the FP8 records added to the default workload's line")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of FP64 oracle time for the cpu_baseline sample")
     args = ap.parse_args(argv)

@@ -253,11 +253,13 @@ int attn_splitkv_default_splits(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, 
  * allocate device memory.  The pages have no counterpart: this is an
  * interface for a kind of caller, not part of the method.
  *
- * Who needs it: code that runs while a CUDA graph is being captured, programs
- * whose device memory is owned by their own pool or arena, and services that
- * forbid allocation on the request path.  attn_fwd_splitkv needs a workspace
- * and the other entry points allocate a status word on their first call on a
- * device; this one allocates nothing.  Its per-split partial results and its
+ * Who needs it: programs whose device memory is owned by their own pool or
+ * arena (a library allocation would compete with it, or fail once the pool
+ * holds the device), and services that forbid allocation on the request path
+ * (an allocation can block, synchronise the device or fail under memory
+ * pressure, breaking their latency and memory bounds).  attn_fwd_splitkv
+ * needs a workspace and the other entry points allocate a status word on
+ * their first call on a device; this one allocates nothing.  Its per-split partial results and its
  * status word live in a fixed device array of 16 MiB that is part of the
  * library (every GPU that loads the library holds it until the process
  * exits).  The caller passes inputs and outputs exactly as for
@@ -275,7 +277,8 @@ int attn_splitkv_default_splits(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, 
  * Sharing: every call on a device uses the same array and it keeps the last
  * call's contents; calls whose kernels overlap on the GPU (for example on two
  * streams) race on it.  A bounded-wait timeout inside its kernels is recorded
- * in the array's status word, which attn_get_status does not read.
+ * in the array's status word; attn_get_status reads and clears it (and
+ * allocates nothing).
  * Errors as attn_fwd_splitkv, plus ATTN_ERR_SCRATCH.
  */
 int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -283,11 +286,13 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
                              float scale, int dtype, void* stream);
 
 /*
- * attn_get_status - synchronise `stream`, then read and clear the device
- * status word that kernels set when a bounded wait expires (ATTN_ERR_TIMEOUT)
- * or an internal check fails (ATTN_ERR_DEVICE).  Returns 0 if no kernel
- * reported a problem since the last call, ATTN_ERR_CUDA if the
- * synchronisation itself failed.
+ * attn_get_status - synchronise `stream`, then read and clear the status
+ * words of the current device that kernels set when a bounded wait expires
+ * (ATTN_ERR_TIMEOUT) or an internal check fails (ATTN_ERR_DEVICE): the word
+ * of the allocating entry points and the one inside the fixed array of
+ * attn_fwd_splitkv_noalloc (each only if set up on this device).  Allocates
+ * nothing.  Returns 0 if no kernel reported a problem since the last call,
+ * ATTN_ERR_CUDA if the synchronisation or a copy failed.
  */
 int attn_get_status(void* stream);
 

@@ -211,6 +211,32 @@ def test_fp8_full_workload_accuracy_and_hadamard(gpu_lib, outlier_scale):
         assert rms[False] <= 5e-2 and rms[True] <= 5e-2, rms
 
 
+def test_fp8_full_workload_every_row_vs_dequantised_oracle(gpu_lib):
+    """B=4, H=16, N=4096, d=128, x50 outliers, with and without the transform,
+    in the bench's launch configuration: all 262,144 rows of the forward
+    against the FP64 oracle run on the oracle's own E4M3 quantisation of the
+    same inputs (the kernel's arithmetic up to the E4M3 rounding of P and the
+    bfloat16 output)."""
+    B, N, H, d = 4, 4096, 16, 128
+    q, k, v = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=0,
+                                outlier_frac=1e-3, device="cuda")
+    sg = synth.hadamard_signs(H, d, seed=0).numpy()
+    cv, dv, _ = ofp8.prepare(v.double().cpu().numpy(), None, False)
+    vdq = ofp8.dequantize(cv, dv)
+    for had in (False, True):
+        o, lse = _fp8_forward(gpu_lib, q, k, v, False, had, H)
+        deq = []
+        for t in (q, k):
+            c, ds, _ = ofp8.prepare(t.double().cpu().numpy(), sg if had else None, had)
+            deq.append(ofp8.dequantize(c, ds))
+        o_ref, lse_ref = oracle.attention_full(deq[0], deq[1], vdq, causal=False,
+                                               scale=1 / math.sqrt(d))
+        e = errors(o, lse, o_ref, lse_ref)
+        assert e["nonfinite"] == 0, (had, e)
+        assert e["o_rel_rms"] <= 4e-2, (had, e)
+        assert e["lse_max_abs"] <= (1e-2 if had else 2e-3), (had, e)
+
+
 # --- per-tensor baseline ------------------------------------------------------
 
 @pytest.mark.parametrize("d", [64, 128, 256])

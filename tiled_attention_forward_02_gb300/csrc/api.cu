@@ -34,32 +34,20 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_launches{0};
 thread_local char g_cuda_msg[256] = "no CUDA error recorded";
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 // one-time per-device set-up; returns 0 or an error code
 int device_state(DeviceState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  int rc = resolve_encoder();
+  if (rc != ATTN_OK) return rc;
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
-    if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) ||
-        (e = cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) ||
-        (e = cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
-        (e = cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
+    if ((rc = device_attrs(dev, &st.sm_count, &st.cc_major, &st.cc_minor)) != ATTN_OK) return rc;
+    if ((e = cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
       return cuda_fail(e, "cudaDeviceGetAttribute");
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-        return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported,
-                         "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
     if ((e = cudaMalloc(&st.status, sizeof(unsigned int))) != cudaSuccess)
       return cuda_fail(e, "cudaMalloc(status word)");
     if ((e = cudaMemset(st.status, 0, sizeof(unsigned int))) != cudaSuccess)
@@ -72,9 +60,33 @@ int device_state(DeviceState** out) {
   return ATTN_OK;
 }
 
+}  // namespace
+
+int resolve_encoder() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode) return ATTN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported,
+                     "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return ATTN_OK;
+}
+
+int device_attrs(int dev, int* sm_count, int* cc_major, int* cc_minor) {
+  cudaError_t e;
+  if ((e = cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev)) ||
+      (e = cudaDeviceGetAttribute(cc_major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+      (e = cudaDeviceGetAttribute(cc_minor, cudaDevAttrComputeCapabilityMinor, dev)))
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  return ATTN_OK;
+}
+
 int encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const cuuint64_t dims[4],
-           const cuuint64_t strides[3], const cuuint32_t box[4],
-           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+           const cuuint64_t strides[3], const cuuint32_t box[4], CUtensorMapSwizzle swizzle) {
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
@@ -90,13 +102,15 @@ int encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const cuu
 // 128 / heads rows (128 rows of 128 bytes in all), `inner` elements of d
 // (128 bytes for the 128-byte swizzle)
 int map_bshd(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* base, int B, int64_t N,
-             int H, int d, int inner, int heads = 1) {
+             int H, int d, int inner, int heads) {
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)d * esz, (cuuint64_t)H * d * esz,
                                  (cuuint64_t)N * H * d * esz};
   const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)heads, (cuuint32_t)(128 / heads), 1};
-  return encode(map, dt, base, dims, strides, box);
+  return encode(map, dt, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
+
+namespace {
 
 // prep input [B, N, H, d] bf16 as dims (d, H, N, B); box = one head's 128 rows
 // of d elements, unswizzled (row r of the tile at r * d * 2 bytes)
@@ -116,10 +130,13 @@ int map_vt(CUtensorMap* map, const void* base, int B, int H, int d, int64_t Npad
   const cuuint64_t strides[3] = {(cuuint64_t)Npad, (cuuint64_t)d * Npad,
                                  (cuuint64_t)H * d * Npad};
   const cuuint32_t box[4] = {128, (cuuint32_t)d, 1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box);
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// checks shared by both forward entry points; returns 1 for an empty problem
+}  // namespace
+
+// checks shared by the forward entry points; returns 1 for an empty problem
 int check_common(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int causal, float scale) {
   if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
@@ -132,8 +149,8 @@ int check_common(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int causal, flo
 }
 
 int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, float scale,
-                const DeviceState& st, int* grid, int n_splits = 1, int split_tiles = 0,
-                int pack_g = 1) {
+                int sm_count, unsigned int* status, int* grid, int n_splits, int split_tiles,
+                int pack_g) {
   const int qst = fwd_q_tiles(d);
   // pack_g query heads share each tile: Nq * pack_g packed rows per head group
   const int64_t n_mb = (Nq * pack_g + qst * 128 - 1) / (qst * 128);
@@ -151,16 +168,14 @@ int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t
   p.nqb = (int)((Nq + 127) / 128);
   p.nkb = (int)((Nk + 127) / 128);
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.status = st.status;
+  p.status = status;
   p.active_stages = (Nq * pack_g <= 128) ? 1 : qst;   // a second tile would hold only padding
   p.pack_g = pack_g;
   p.n_splits = n_splits;
   p.split_tiles = split_tiles > 0 ? split_tiles : p.n_kv_tiles;
-  *grid = (int)(units < st.sm_count ? units : st.sm_count);
+  *grid = (int)(units < sm_count ? units : sm_count);
   return ATTN_OK;
 }
-
-}  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
@@ -202,14 +217,15 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
   if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64, pack_g)) ||
-      (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64)) ||
-      (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64)))
+      (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64, 1)) ||
+      (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64, 1)))
     return rc;
   FwdParams p{};
   p.o = o;
   p.lse = lse;
   int grid = 0;
-  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid, 1, 0, pack_g)) != ATTN_OK)
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, st->sm_count, st->status, &grid, 1, 0,
+                        pack_g)) != ATTN_OK)
     return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int mode = pack_g > 1 ? 2 : causal;
@@ -238,8 +254,8 @@ extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
   const int64_t Npad = (Nk + 15) / 16 * 16;
   CUtensorMap mq, mk, mv;
-  if ((rc = map_bshd(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q8, B, Nq, Hq, d, 128)) ||
-      (rc = map_bshd(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k8, B, Nk, Hkv, d, 128)) ||
+  if ((rc = map_bshd(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q8, B, Nq, Hq, d, 128, 1)) ||
+      (rc = map_bshd(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k8, B, Nk, Hkv, d, 128, 1)) ||
       (rc = map_vt(&mv, v8t, B, Hkv, d, Npad)))
     return rc;
   FwdParams p{};
@@ -249,7 +265,9 @@ extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
   p.k_descale = k_descale;
   p.v_descale = v_descale;
   int grid = 0;
-  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid)) != ATTN_OK) return rc;
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, st->sm_count, st->status, &grid, 1, 0,
+                        1)) != ATTN_OK)
+    return rc;
   return launch_fwd_e4m3(d, causal, mq, mk, mv, p, grid, static_cast<cudaStream_t>(stream));
 }
 
@@ -340,7 +358,7 @@ int splitkv_pack(int group, int eff_splits, int64_t Nq, int d) {
 }
 }  // namespace attn
 
-namespace {
+namespace attn {
 // key tiles per split and the number of non-empty splits for a request
 void split_layout(int64_t Nk, int num_splits, int* split_tiles, int* eff_splits) {
   const int tiles = (int)((Nk + 127) / 128);
@@ -351,11 +369,14 @@ void split_layout(int64_t Nk, int num_splits, int* split_tiles, int* eff_splits)
 }
 
 int64_t splitkv_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, int64_t splits) {
-  const int64_t rows = splits * B * Hq * Nq;
-  const int64_t o_bytes = (rows * d * 4 + 255) / 256 * 256;   // LSE part starts 256-aligned
-  return o_bytes + rows * 4;
+  return splitkv_lse_offset(B, Hq, Nq, d, splits) + splits * B * Hq * Nq * 4;
 }
-}  // namespace
+
+int64_t splitkv_lse_offset(int64_t B, int64_t Hq, int64_t Nq, int64_t d, int64_t splits) {
+  const int64_t rows = splits * B * Hq * Nq;
+  return (rows * d * 4 + 255) / 256 * 256;   // the LSE part starts 256-byte aligned
+}
+}  // namespace attn
 
 extern "C" size_t attn_splitkv_workspace_bytes(int B, int Hq, int64_t Nq, int d, int num_splits) {
   if (B < 0 || Hq < 1 || Nq < 0 || d < 1 || num_splits < 1) return 0;
@@ -412,23 +433,22 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
       dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv;
   if ((rc = map_bshd(&mq, tdt, 2, q, B, Nq, Hq, d, 64, pack_g)) ||
-      (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64)) ||
-      (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64)))
+      (rc = map_bshd(&mk, tdt, 2, k, B, Nk, Hkv, d, 64, 1)) ||
+      (rc = map_bshd(&mv, tdt, 2, v, B, Nk, Hkv, d, 64, 1)))
     return rc;
   FwdParams p{};
   p.o = o;
   p.lse = lse;
   int grid = 0;
-  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, *st, &grid, eff, split_tiles, pack_g)) !=
-      ATTN_OK)
+  if ((rc = fill_params(p, d, B, Hq, Hkv, Nq, Nk, scale, st->sm_count, st->status, &grid, eff,
+                        split_tiles, pack_g)) != ATTN_OK)
     return rc;
   float* o_part = nullptr;
   float* lse_part = nullptr;
   if (eff > 1) {
-    const int64_t rows = (int64_t)eff * B * Hq * Nq;
     o_part = static_cast<float*>(workspace);
     lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        (rows * d * 4 + 255) / 256 * 256);
+                                        splitkv_lse_offset(B, Hq, Nq, d, eff));
   }
   p.o_part = o_part;
   p.lse_part = lse_part;
@@ -443,17 +463,31 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
 }
 
 extern "C" int attn_get_status(void* stream) {
-  DeviceState* st = nullptr;
-  int rc = device_state(&st);
-  if (rc != ATTN_OK) return rc;
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  if ((e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "cudaStreamSynchronize");
+  // the allocated status word, if an allocating entry point set it up
+  unsigned int* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_dev[dev].ready) status = g_dev[dev].status;
+  }
   unsigned int word = 0;
-  if ((e = cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
-    return cuda_fail(e, "cudaMemcpy(status word)");
+  if (status) {
+    if ((e = cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy(status word)");
+    if (word != 0 && (e = cudaMemset(status, 0, sizeof(word))) != cudaSuccess)
+      return cuda_fail(e, "cudaMemset(status word)");
+  }
+  // the no-alloc entry point's status word (inside its fixed array)
+  unsigned int na_word = 0;
+  int rc = noalloc_take_status(dev, &na_word);
+  if (rc != ATTN_OK) return rc;
+  word |= na_word;
   if (word == 0) return ATTN_OK;
-  if ((e = cudaMemset(st->status, 0, sizeof(word))) != cudaSuccess)
-    return cuda_fail(e, "cudaMemset(status word)");
   return (word & kStatusTimeout) ? ATTN_ERR_TIMEOUT : ATTN_ERR_DEVICE;
 }
 

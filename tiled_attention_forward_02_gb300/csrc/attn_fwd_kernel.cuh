@@ -168,7 +168,6 @@ __device__ __forceinline__ void issue_s_mmas(uint32_t tS, uint32_t qlo, uint32_t
    ...);
 }
 // O += P V with P read from tensor memory (8 columns per MMA) and the V tile
-// advancing by VSTEP bytes per MMA
 // advancing by VSTEP bytes per MMA; FIRST: the unit's first PV overwrites O
 template <int DT, int VSTEP, bool FIRST, size_t... KK>
 __device__ __forceinline__ void issue_pv_mmas(uint32_t tO, uint32_t tS, uint32_t vlo, uint32_t idO,

@@ -32,6 +32,34 @@ int launch_fwd_e4m3(int d, int causal, const CUtensorMap& q, const CUtensorMap& 
 // query tiles per work unit of the fused forward (tensor-memory budget)
 inline int fwd_q_tiles(int d) { return d == 256 ? 1 : 2; }
 
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// --- host helpers that allocate nothing (api.cu); the no-alloc entry point
+// uses them too
+// resolves cuTensorMapEncodeTiled once per process
+int resolve_encoder();
+// number of SMs and compute capability of device `dev`
+int device_attrs(int dev, int* sm_count, int* cc_major, int* cc_minor);
+// argument checks of the forward entry points; 1 for an empty problem
+int check_common(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int causal, float scale);
+// BSHD tensor [B, N, H, d] as a 4-D tensor map (d, H, N, B) with a box of
+// `heads` heads x 128 / heads rows x `inner` elements, 128-byte swizzle
+int map_bshd(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* base, int B, int64_t N,
+             int H, int d, int inner, int heads);
+// forward parameters and persistent grid size for a problem
+int fill_params(FwdParams& p, int d, int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, float scale,
+                int sm_count, unsigned int* status, int* grid, int n_splits, int split_tiles,
+                int pack_g);
+// key tiles per split and the number of non-empty splits for a request
+void split_layout(int64_t Nk, int num_splits, int* split_tiles, int* eff_splits);
+// bytes of split partial results (O / l rows, then LSE rows from a 256-byte
+// aligned offset)
+int64_t splitkv_bytes(int64_t B, int64_t Hq, int64_t Nq, int64_t d, int64_t splits);
+int64_t splitkv_lse_offset(int64_t B, int64_t Hq, int64_t Nq, int64_t d, int64_t splits);
+// reads and clears the no-alloc entry point's status word of device `dev`
+// (0 if that entry point was never set up there); allocates nothing
+int noalloc_take_status(int dev, unsigned int* word);
+
 // query heads the split instance packs into a tile's rows (api.cu)
 int splitkv_pack(int group, int eff_splits, int64_t Nq, int d);
 

@@ -47,11 +47,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// barrier `id` (1..15) among `count` threads of the CTA (a multiple of 32)
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // like mbar_try_wait, but the thread may sleep in hardware for up to
 // `suspend_ns` (waking when the phase completes) instead of returning at once
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
@@ -97,12 +92,6 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 
