@@ -107,10 +107,14 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *                                  FP8 P V product reads (the pages' V
  *                                  transpose, section 7.4).
  *   descale  [B, H, ceil(N/128)] float32 (written): one scale per block of
- *            128 tokens x d of one (b, head); descale = amax / 448, or 1 for
- *            an all-zero block.  code = E4M3_RNE_satfinite(y * r) with
- *            r = 448 / amax rounded to float32 once per block (1 for an
- *            all-zero block) and the product rounded to float32.
+ *            128 tokens x d of one (b, head); descale = amax / 448 rounded
+ *            to float32, or 1 for an all-zero block.
+ *            code = E4M3 of y / descale, round-to-nearest-even, saturated to
+ *            +-448.  Without the transform (y = x) the code is that of the
+ *            exact quotient, ties included.  With the transform, y is formed
+ *            in float32 and scaled by r = 448 / amax (float32, once per
+ *            block) times 1 / sqrt(d): a code may then differ by one step
+ *            where y / descale lies within float32 rounding of a midpoint.
  *   signs    NULL (no transform) or [sign_heads, d] int8 of +1/-1 (device).
  *            With signs, every row is replaced, before quantisation, by
  *            y = (x * sigma) H_d / sqrt(d) in float32, H_d the Sylvester
@@ -134,8 +138,8 @@ int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int64_t
  *   descale  [B, H, ceil(N/128)] float32 (written): every entry equals
  *            amax / 448 with amax over the whole tensor after the transform
  *            (1 for an all-zero tensor), so attn_fwd_fp8 consumes it
- *            unchanged.  code = E4M3_RNE_satfinite(y * r), r = 448 / amax
- *            rounded to float32 once.  descale[0] serves as the amax
+ *            unchanged.  Codes as attn_prep_fp8 with that one descale.
+ *            descale[0] serves as the amax
  *            accumulator while the call runs (three kernels and a 4-byte
  *            memset on `stream`).
  *   Returns as attn_prep_fp8.
