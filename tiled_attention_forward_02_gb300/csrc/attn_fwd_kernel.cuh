@@ -123,19 +123,20 @@ struct FwdCfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int S_COL0 = 0;                  // S_s at S_COL0 + 128 s
   static constexpr int O_COL0 = 128 * QST;          // O_s at O_COL0 + D s
-  // two query tiles: 2 softmax warpgroups + one warpgroup holding the MMA and
-  // TMA warps (and two idle warps) so registers can move between warpgroups;
-  // split rows: 4 softmax warpgroups + the MMA and TMA warps, no register split
-  static constexpr int NUM_WARPS = SPLITROW ? NSOFT + 2 : (QST == 2) ? 12 : 6;
+  // two query tiles: 2 (split rows: 4) softmax warpgroups + one warpgroup
+  // holding the MMA and TMA warps (and two idle warps) so that registers can
+  // move between warpgroups
+  static constexpr int NUM_WARPS = (QST == 2) ? NSOFT + 4 : 6;
   static constexpr int NTHREADS = NUM_WARPS * 32;
   static constexpr int W_MMA = NSOFT;
   static constexpr int W_LOAD = NSOFT + 1;
-  // register split (setmaxnreg) of the two-tile layout; the launch must give
+  // register split (setmaxnreg) of the two-tile layouts; the launch must give
   // each thread at least LAUNCH_REGS so that the split fits in the block's pool
-  static constexpr bool REGSPLIT = (QST == 2) && !SPLITROW;
-  static constexpr int REG_SOFTMAX = 216;
-  static constexpr int REG_OTHER = 72;
-  static constexpr int LAUNCH_REGS = (2 * REG_SOFTMAX + REG_OTHER + 2) / 3;
+  static constexpr bool REGSPLIT = (QST == 2);
+  static constexpr int REG_SOFTMAX = SPLITROW ? 104 : 216;
+  static constexpr int REG_OTHER = SPLITROW ? 56 : 72;
+  static constexpr int LAUNCH_REGS =
+      (NSOFT * 32 * REG_SOFTMAX + (NUM_WARPS - NSOFT) * 32 * REG_OTHER + NTHREADS - 1) / NTHREADS;
   // softmax: lazy rescale threshold (log2 units) and exponent shift of P
   static constexpr float TAU = (DT == DT_E4M3) ? 2.0f : 8.0f;
   static constexpr float PSHIFT = (DT == DT_E4M3) ? 6.0f : 0.0f;
@@ -322,16 +323,8 @@ __device__ __forceinline__ void octet_transpose(uint32_t (&w)[32], int lane) {
 }
 
 // --------------------------------------------------------------------- kernel
-// Register cap per thread: the split-row layout (18 warps) takes 112 (18 x 32
-// x 112 fits the SM's 64 K registers; a thread-count bound alone would let
-// the compiler assume less), the others the launch bound of their block.
-template <int D, int DT>
-constexpr int fwd_max_regs() {
-  return FwdCfg<D, DT>::SPLITROW ? 112 : (65536 / FwdCfg<D, DT>::NTHREADS) / 8 * 8;
-}
-
 template <int D, int DT, bool CAUSAL, bool SPLIT>
-__global__ void __maxnreg__((fwd_max_regs<D, DT>()))
+__global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D, DT>;
@@ -848,6 +841,7 @@ __global__ void __maxnreg__((fwd_max_regs<D, DT>()))
     __syncwarp();
   } else if (warp < C::NSOFT && C::SPLITROW) {
     if constexpr (C::SPLITROW) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
     // ============================================ softmax, rows split in two
     // Warp w: query tile s = (w >> 2) & 1, key-column half hf = w >> 3 (keys
     // 64 hf .. 64 hf + 63 of every key tile), TMEM lane quarter w & 3; its
