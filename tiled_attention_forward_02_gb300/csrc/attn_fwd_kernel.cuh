@@ -106,37 +106,24 @@ struct FwdCfg {
   static constexpr bool PSMEM = (DT == DT_E4M3) && (QST == 2);
   static constexpr int PBYTES = BM * BN * ELT;      // one P tile (K-major, 128-byte swizzle)
   static constexpr int PTOTAL = PSMEM ? QST * 2 * PBYTES : 0;   // two buffers per query tile
-  // The same instance splits the 128 key columns of each row of S over two
-  // softmax warps (keys 0-63 and 64-127 of every tile): four softmax warps
-  // per SM sub-partition instead of two, each with half the dependent chain.
-  // The two warps of a row exchange their half maxima (and, at the end of a
-  // unit, their half sums) through shared memory: [tile][slot][half][row].
-  static constexpr bool SPLITROW = PSMEM;
-  static constexpr int XBYTES = SPLITROW ? 2 * 2 * 2 * BM * 4 : 0;
-  static constexpr int WARPS_PER_TILE = SPLITROW ? 8 : 4;   // softmax warps of one query tile
-  static constexpr int NSOFT = QST * WARPS_PER_TILE;
   static constexpr int SLOT_FIT =
-      (SMEM_LIMIT - 1024 - SMEM_TAIL - QST * QBYTES - PTOTAL - XBYTES) / KVBYTES;
+      (SMEM_LIMIT - 1024 - SMEM_TAIL - QST * QBYTES - PTOTAL) / KVBYTES;
   static constexpr int NSLOT = SLOT_FIT > 8 ? 8 : SLOT_FIT;
-  static constexpr int SMEM_BYTES =
-      1024 + QST * QBYTES + PTOTAL + XBYTES + NSLOT * KVBYTES + SMEM_TAIL;
+  static constexpr int SMEM_BYTES = 1024 + QST * QBYTES + PTOTAL + NSLOT * KVBYTES + SMEM_TAIL;
   static constexpr int TMEM_COLS = 512;
   static constexpr int S_COL0 = 0;                  // S_s at S_COL0 + 128 s
   static constexpr int O_COL0 = 128 * QST;          // O_s at O_COL0 + D s
-  // two query tiles: 2 (split rows: 4) softmax warpgroups + one warpgroup
-  // holding the MMA and TMA warps (and two idle warps) so that registers can
-  // move between warpgroups
-  static constexpr int NUM_WARPS = (QST == 2) ? NSOFT + 4 : 6;
+  // two query tiles: 2 softmax warpgroups + one warpgroup holding the MMA and
+  // TMA warps (and two idle warps) so registers can move between warpgroups
+  static constexpr int NUM_WARPS = (QST == 2) ? 12 : 6;
   static constexpr int NTHREADS = NUM_WARPS * 32;
-  static constexpr int W_MMA = NSOFT;
-  static constexpr int W_LOAD = NSOFT + 1;
-  // register split (setmaxnreg) of the two-tile layouts; the launch must give
+  static constexpr int W_MMA = QST * 4;
+  static constexpr int W_LOAD = QST * 4 + 1;
+  // register split (setmaxnreg) of the two-tile layout; the launch must give
   // each thread at least LAUNCH_REGS so that the split fits in the block's pool
-  static constexpr bool REGSPLIT = (QST == 2);
-  static constexpr int REG_SOFTMAX = SPLITROW ? 104 : 216;
-  static constexpr int REG_OTHER = SPLITROW ? 56 : 72;
-  static constexpr int LAUNCH_REGS =
-      (NSOFT * 32 * REG_SOFTMAX + (NUM_WARPS - NSOFT) * 32 * REG_OTHER + NTHREADS - 1) / NTHREADS;
+  static constexpr int REG_SOFTMAX = 216;
+  static constexpr int REG_OTHER = 72;
+  static constexpr int LAUNCH_REGS = (2 * REG_SOFTMAX + REG_OTHER + 2) / 3;
   // softmax: lazy rescale threshold (log2 units) and exponent shift of P
   static constexpr float TAU = (DT == DT_E4M3) ? 2.0f : 8.0f;
   static constexpr float PSHIFT = (DT == DT_E4M3) ? 6.0f : 0.0f;
@@ -338,10 +325,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   static_assert(!(C::PSMEM && SPLIT), "split instances keep P in tensor memory");
   const uint32_t sQ = sraw + pad;                       // QST query tiles
   const uint32_t sP = sQ + QST * C::QBYTES;             // P tiles (shared-memory P only)
-  const uint32_t sX = sP + C::PTOTAL;                   // row-max / row-sum exchange (split rows)
-  const uint32_t sKV = sX + C::XBYTES;                  // NSLOT K/V slots
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + QST * C::QBYTES + C::PTOTAL + C::XBYTES +
-                                               NSLOT * C::KVBYTES);
+  const uint32_t sKV = sP + C::PTOTAL;                  // NSLOT K/V slots
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + QST * C::QBYTES + C::PTOTAL + NSLOT * C::KVBYTES);
 
   // barrier table
   constexpr int B_QFULL = 0;                 // [2]   TMA Q landed            (tx)
@@ -357,9 +343,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   constexpr int B_SFREE = B_DRAIN + 1;       // [2]   S_s read into registers (4 warp arrivals)
   constexpr int B_PFULLB = B_SFREE + 2;      // [2x2] P buffer written      (4 warp arrivals)
   constexpr int B_PFREEB = B_PFULLB + 4;     // [2x2] PV done reading it    (commit)
-  // split rows: exchange of the two warps of (tile s, lane quarter q), entry 4 s + q
-  constexpr int B_XCH = B_PFREEB + 4;        // [8]   both halves posted     (2 warp arrivals)
-  constexpr int NBARS = B_XCH + 8;
+  constexpr int NBARS = B_PFREEB + 4;
   static_assert(NBARS * 8 + 16 <= C::SMEM_TAIL, "barrier table too large");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -379,7 +363,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       ptx::mbar_init(bar(B_SFULL + s), 1);
       ptx::mbar_init(bar(B_PFULL + s), 4);   // one elected arrival per softmax warp
       ptx::mbar_init(bar(B_OFULL + s), 1);
-      ptx::mbar_init(bar(B_OEMPTY + s), C::WARPS_PER_TILE);
+      ptx::mbar_init(bar(B_OEMPTY + s), 4);
     }
     ptx::mbar_init(bar(B_QEMPTY), 1);
     for (int i = 0; i < NSLOT; ++i) {
@@ -387,12 +371,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       ptx::mbar_init(bar(B_KVEMPTY + i), 1);
     }
     ptx::mbar_init(bar(B_DRAIN), 1);
-    for (int s = 0; s < 2; ++s) ptx::mbar_init(bar(B_SFREE + s), C::WARPS_PER_TILE);
+    for (int s = 0; s < 2; ++s) ptx::mbar_init(bar(B_SFREE + s), 4);
     for (int i = 0; i < 4; ++i) {
-      ptx::mbar_init(bar(B_PFULLB + i), C::WARPS_PER_TILE);
+      ptx::mbar_init(bar(B_PFULLB + i), 4);
       ptx::mbar_init(bar(B_PFREEB + i), 1);
     }
-    for (int i = 0; i < 8; ++i) ptx::mbar_init(bar(B_XCH + i), 2);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -412,7 +395,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
 
   if (warp == C::W_LOAD) {
     // ===================================================== TMA producer
-    if constexpr (C::REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
+    if constexpr (QST == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
     if (lane == 0) {
       int kv_it = 0, u_it = 0;
       bool ok = true;
@@ -474,7 +457,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     __syncwarp();
   } else if (warp == C::W_MMA) {
     // ===================================================== MMA issuer
-    if constexpr (C::REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
+    if constexpr (QST == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
     if (lane == 0) {
       constexpr uint32_t fmt = (DT == DT_BF16) ? 1u : 0u;
       constexpr uint32_t idS = idesc_make(fmt, 128, 128, false);
@@ -839,250 +822,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       wait_bar(bar(B_DRAIN), 0, Ctl{abort_flag, p.status});
     }
     __syncwarp();
-  } else if (warp < C::NSOFT && C::SPLITROW) {
-    if constexpr (C::SPLITROW) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
-    // ============================================ softmax, rows split in two
-    // Warp w: query tile s = (w >> 2) & 1, key-column half hf = w >> 3 (keys
-    // 64 hf .. 64 hf + 63 of every key tile), TMEM lane quarter w & 3; its
-    // partner (same tile and rows, other half) is warp w ^ 8, on the same SM
-    // sub-partition. Both keep the row's reference maximum (identical) and a
-    // sum over their own half; O columns are split the same way for the
-    // rescale and the epilogue.
-    const int s = (warp >> 2) & 1;
-    const int hf = warp >> 3;
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::S_COL0 + 128 * s + 64 * hf;
-    const uint32_t tO = tmem + lane_off + C::O_COL0 + D * s + (D / 2) * hf;
-    const uint32_t prow0 = sP + 2 * s * C::PBYTES + (r >> 3) * 1024 + (r & 7) * 128;
-    float* xbuf = reinterpret_cast<float*>(smem + (sX - sQ));
-    const uint32_t xbar = bar(B_XCH + s * 4 + quarter);
-    int xc = 0;   // exchanges made with the partner; slot xc % 2, mbarrier phase xc
-    // post `mine` for this thread's row, wait (bounded) until the partner has
-    // posted its value for the same exchange, return it in `other`. Slot n % 2
-    // is written again only at exchange n + 2, after both warps completed
-    // exchange n + 1, i.e. after the partner read it at exchange n.
-    auto exchange = [&](float mine, float& other) -> bool {
-      float* slot = xbuf + (s * 2 + (xc & 1)) * (2 * C::BM);
-      slot[hf * C::BM + r] = mine;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(xbar);
-      const bool okx = warp_wait_bar(xbar, xc & 1, ctl);
-      other = slot[(1 - hf) * C::BM + r];
-      ++xc;
-      return okx;
-    };
-    int s_cnt = 0, u_it = 0, p_cnt = 0;
-    bool ok = true;
-    for (int it = 0; ok; ++it) {
-      const int u = unit_of_round<CAUSAL>(it, p);
-      if (u == -2) break;
-      if (u < 0) continue;
-      const Unit U = decode_unit<QST, CAUSAL, SPLIT>(u, p);
-      const int m_s = U.m0 + s * 128;   // first query position of this tile
-      const int row = m_s + r;
-      const int ns = U.n_s[s];
-
-      const int qb = m_s >> 7;
-      const float qd =
-          (qb < p.nqb) ? __ldg(p.q_descale + ((long long)U.b * p.Hq + U.hq) * p.nqb + qb) : 1.f;
-      const float* kd_row = p.k_descale + ((long long)U.b * p.Hkv + U.hk) * p.nkb;
-      const float* vd_row = p.v_descale + ((long long)U.b * p.Hkv + U.hk) * p.nkb;
-      float vm = 0.f;
-      for (int t = lane; t < p.nkb; t += 32) vm = fmaxf(vm, __ldg(vd_row + t));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-      const float vref = vm > 0.f ? vm : 1.f;
-
-      float mi = -CUDART_INF_F;   // reference maximum of the scaled logits (log2 units)
-      float li = 0.f;             // sum over this half of exp2(logit - mi)
-      // per-tile factors (logit scale, exponent bias, sum scale) one tile ahead
-      const float cq = p.scale_log2 * qd;
-      const float lvref = ptx::lg2(vref);
-      auto fp8_factors = [&](float kd, float vd, float& cjo, float& bo, float& sso) {
-        const float lr = ptx::lg2(vd) - lvref;   // log2 of V block scale / largest, <= 0
-        cjo = cq * kd;
-        bo = C::PSHIFT + lr;
-        sso = ptx::ex2(-lr);
-      };
-      float cj_cur, bias_cur, ssc_cur, kd_next = 1.f, vd_next = 1.f;
-      fp8_factors(__ldg(kd_row + U.j0), __ldg(vd_row + U.j0), cj_cur, bias_cur, ssc_cur);
-      if (ns > 1) {
-        kd_next = __ldg(kd_row + U.j0 + 1);
-        vd_next = __ldg(vd_row + U.j0 + 1);
-      }
-      for (int j = 0; j < ns; ++j) {
-        ok = warp_wait_bar(bar(B_SFULL + s), s_cnt & 1, ctl);
-        ++s_cnt;
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const int n0 = (U.j0 + j) * 128 + 64 * hf;   // first key of this half
-        const bool masked = (n0 + 64 > p.Nk) || (CAUSAL && n0 + 63 > m_s);
-        uint32_t sr[64];
-        float hmax;
-        if (!masked) ptx::tmem_ld_max_x64(tS, sr, hmax);
-        else ptx::tmem_ld_x64(tS, sr);
-        // S_s is in registers (both halves once the partner arrives too)
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(B_SFREE + s));
-        float sv[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(sr[c]);
-        if (masked) {
-          int lim = p.Nk - n0;
-          if (CAUSAL) lim = min(lim, row - n0 + 1);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = (c < lim) ? sv[c] : -CUDART_INF_F;
-          float mx[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            mx[i] = ptx::max3(sv[i], sv[i + 8], sv[i + 16]);
-            mx[i] = ptx::max3(mx[i], sv[i + 24], sv[i + 32]);
-            mx[i] = ptx::max3(mx[i], sv[i + 40], sv[i + 48]);
-            mx[i] = fmaxf(mx[i], sv[i + 56]);
-          }
-          hmax = fmaxf(ptx::max3(ptx::max3(mx[0], mx[1], mx[2]), ptx::max3(mx[3], mx[4], mx[5]),
-                                 mx[6]),
-                       mx[7]);
-        }
-        float omax;
-        ok = exchange(hmax, omax);
-        if (!ok) break;
-        const float rmax = fmaxf(hmax, omax);   // the same float in both warps
-
-        const float cj = cj_cur, bias_extra = bias_cur, sum_scale = ssc_cur;
-        const float m_new = fmaxf(mi, rmax * cj);
-        float alpha = 1.f;
-        bool rescale = false;
-        if (j == 0) {
-          mi = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-        } else if (m_new > mi + C::TAU) {
-          // the new maximum exceeds the reference by more than 2^TAU: move
-          // the reference (merge rule of section 4.2), rescale O and l
-          alpha = ptx::ex2(mi - m_new);
-          mi = m_new;
-          li *= alpha;
-          rescale = true;
-        }
-        // buffer p_cnt % 2 is free once PV number p_cnt - 2 is done; O_s holds
-        // every previous PV product (needed before a rescale) once PV number
-        // p_cnt - 1 is done. Both warps of a row take the same decisions.
-        const bool any_rescale = __any_sync(0xffffffffu, rescale);
-        const int wait_n = any_rescale ? p_cnt - 1 : p_cnt - 2;
-        if (wait_n >= 0) {
-          ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (wait_n & 1)), (wait_n >> 1) & 1, ctl);
-          if (!ok) break;
-          ptx::tc_fence_after();
-        }
-        if (any_rescale) {
-#pragma unroll 1
-          for (int cb = 0; cb < D / 2; cb += 32) {
-            uint32_t o32[32];
-            ptx::tmem_ld_x32(tO + cb, o32);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o32[c] = __float_as_uint(__uint_as_float(o32[c]) * alpha);
-            ptx::tmem_st_x32(tO + cb, o32);
-          }
-        }
-
-        // P = exp2(logit - reference) of this half, its sum, E4M3 codes into
-        // chunks 4 hf .. 4 hf + 3 of the row (K-major, 128-byte swizzle)
-        const float nbias = bias_extra - mi;
-        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-        const uint32_t prow = prow0 + (uint32_t)(p_cnt & 1) * C::PBYTES;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-#pragma unroll
-          for (int c = 32 * k; c < 32 * k + 32; c += 4) {
-            float x0, x1, x2, x3;
-            ptx::fma2(x0, x1, sv[c], sv[c + 1], cj, cj, nbias, nbias);
-            ptx::fma2(x2, x3, sv[c + 2], sv[c + 3], cj, cj, nbias, nbias);
-            sv[c] = ptx::ex2(x0);
-            sv[c + 1] = ptx::ex2(x1);
-            sv[c + 2] = ptx::ex2(x2);
-            sv[c + 3] = ptx::ex2(x3);
-            ptx::add2(sum0, sum1, sv[c], sv[c + 1]);
-            ptx::add2(sum2, sum3, sv[c + 2], sv[c + 3]);
-          }
-          uint32_t pk[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int e = 32 * k + 4 * c;
-            pk[c] = ptx::pack_e4m3x4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
-          }
-          const int ch = 4 * hf + 2 * k;
-          ptx::st_shared_v4(prow + ((ch ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
-          ptx::st_shared_v4(prow + (((ch + 1) ^ (r & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
-        }
-        li += ((sum0 + sum1) + (sum2 + sum3)) * sum_scale;
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        ptx::fence_proxy_async_smem();   // P visible to the MMA
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(B_PFULLB + 2 * s + (p_cnt & 1)));
-        ++p_cnt;
-        if (j + 1 < ns) {
-          fp8_factors(kd_next, vd_next, cj_cur, bias_cur, ssc_cur);
-          if (j + 2 < ns) {
-            kd_next = __ldg(kd_row + U.j0 + j + 2);
-            vd_next = __ldg(vd_row + U.j0 + j + 2);
-          }
-        }
-      }
-      if (!ok) break;
-
-      // ------------------------------------------------------------ epilogue
-      ok = warp_wait_bar(bar(B_OFULL + s), u_it & 1, ctl);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      float lother;
-      ok = exchange(li, lother);
-      if (!ok) break;
-      const float lt = li + lother;   // the row's sum over both halves
-      const float inv = vref / lt;
-      // l carries the factor 2^PSHIFT of the FP8 instance
-      const float lse_row = (mi + ptx::lg2(lt) - C::PSHIFT) * 0.6931471805599453f;
-      // this warp's 64 columns of O: after an 8 x 8 transpose of 16-byte
-      // pieces inside each lane octet every store writes whole 128-byte lines
-      const int rb = 32 * quarter + 8 * (lane >> 3);
-      const int pc = lane & 7;
-      uint16_t* obase = reinterpret_cast<uint16_t*>(p.o);
-      const int cb = (D / 2) * hf;
-      {
-        uint32_t w[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {   // two 32-column loads, packed as they arrive
-          uint32_t o32[32];
-          ptx::tmem_ld_x32(tO + 32 * h, o32);
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            w[16 * h + c] = ptx::pack_bf16x2(__uint_as_float(o32[2 * c]) * inv,
-                                             __uint_as_float(o32[2 * c + 1]) * inv);
-        }
-        octet_transpose(w, lane);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int pos = m_s + rb + k;
-          if (pos < p.Nq) {
-            uint16_t* dst = obase + (((long long)U.b * p.Nq + pos) * p.Hq + U.hq) * D + cb;
-            reinterpret_cast<uint4*>(dst)[pc] =
-                make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-          }
-        }
-      }
-      if (hf == 0 && row < p.Nq) p.lse[((long long)U.b * p.Hq + U.hq) * p.Nq + row] = lse_row;
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(B_OEMPTY + s));
-      ++u_it;
-    }
-    }
-  } else if (warp < C::NSOFT) {
+  } else if (warp < QST * 4) {
     // ===================================================== softmax warpgroups
-    if constexpr (C::REGSPLIT) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
+    if constexpr (QST == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
     const int s = warp >> 2;           // query tile of this warpgroup
     const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane; // row within the tile
@@ -1213,21 +955,17 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
           li *= alpha;
           rescale = true;
         }
+        const bool any_rescale = __any_sync(0xffffffffu, rescale);
         if constexpr (C::PSMEM) {
-          // the P buffer is free, and O_s holds the previous PV product, once
-          // the previous PV GEMM of this tile is done
-          // buffer p_cnt % 2 is free once PV number p_cnt - 2 is done; O_s holds
-          // every previous PV product (needed before a rescale) once PV
-          // number p_cnt - 1 is done
-          const bool any_rescale = __any_sync(0xffffffffu, rescale);
-          const int wait_n = any_rescale ? p_cnt - 1 : p_cnt - 2;
-          if (wait_n >= 0) {
-            ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (wait_n & 1)), (wait_n >> 1) & 1, ctl);
+          // P buffer p_cnt % 2 is free once PV number p_cnt - 2 is done; a
+          // rescale of O waits until after P is written (below)
+          if (p_cnt >= 2) {
+            const int n = p_cnt - 2;
+            ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
             if (!ok) break;
             ptx::tc_fence_after();
           }
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
+        } else if (any_rescale) {
 #pragma unroll 1
           for (int cb = 0; cb < D; cb += 32) {
             uint32_t o32[32];
@@ -1284,6 +1022,40 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
           }
         }
         li += ((sum0 + sum1) + (sum2 + sum3)) * sum_scale;
+        if constexpr (C::PSMEM) {
+          if (any_rescale) {
+            // P is already relative to the moved reference; O_s holds every
+            // previous PV product once PV number p_cnt - 1 is done (it had the
+            // whole exponential phase to finish). The S registers are dead:
+            // O is read 64 columns at a time with both loads in flight.
+            const int n = p_cnt - 1;
+            ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            static_assert(D % 128 == 0, "O rescale in pairs of 64-column loads");
+#pragma unroll 1
+            for (int cb = 0; cb < D; cb += 128) {
+              uint32_t oa[64], ob[64];
+              ptx::tmem_ld_x64_nowait(tO + cb, oa);
+              ptx::tmem_ld_x64_nowait(tO + cb + 64, ob);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 64; c += 2) {
+                float a0, a1, b0, b1;
+                ptx::fma2(a0, a1, __uint_as_float(oa[c]), __uint_as_float(oa[c + 1]), alpha, alpha,
+                          0.f, 0.f);
+                ptx::fma2(b0, b1, __uint_as_float(ob[c]), __uint_as_float(ob[c + 1]), alpha, alpha,
+                          0.f, 0.f);
+                oa[c] = __float_as_uint(a0);
+                oa[c + 1] = __float_as_uint(a1);
+                ob[c] = __float_as_uint(b0);
+                ob[c + 1] = __float_as_uint(b1);
+              }
+              ptx::tmem_st_x64(tO + cb, oa);
+              ptx::tmem_st_x64(tO + cb + 64, ob);
+            }
+          }
+        }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         if constexpr (C::PSMEM) ptx::fence_proxy_async_smem();   // P visible to the MMA
@@ -1393,7 +1165,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     }
   } else {
     // idle warps of the MMA/TMA warpgroup
-    if constexpr (C::REGSPLIT) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
+    if constexpr (QST == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
   }
 
   // --------------------------------------------------------------- teardown

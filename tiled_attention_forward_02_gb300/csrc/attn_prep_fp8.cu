@@ -20,10 +20,10 @@
 // shuffles across the LPR lanes of the row), scaled by 1/sqrt(d); the
 // block amax is reduced through shared memory; descale = amax / 448 (float32);
 // codes are the E4M3 rounding (nearest-even, saturated to +-448) of y /
-// descale: exactly that of the quotient when y is the input itself (two
-// bracketing float32 products, and an exact residual test when a rounding
-// boundary lies between them), else of y * (448 / amax) with the reciprocal
-// rounded once per block.  It
+// descale: exactly that of the quotient when y is the input itself (one
+// product with a per-block reciprocal nudged to the exact quotient's side of
+// every rounding midpoint, see the quantisation step), else of y * (448 /
+// amax) with the reciprocal rounded once per block.  It
 // reads each bf16 element once and writes one byte per element, an HBM-bound
 // amount of work; at two CTAs of 8 warps per SM (register and shared-memory
 // limits) the kernel itself is bound by instruction latency, not bandwidth.
@@ -59,47 +59,6 @@ __device__ __forceinline__ void load_chunk(uint32_t saddr, float* y) {
     y[2 * i] = __uint_as_float(ws[i] << 16);
     y[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
   }
-}
-
-// value of an E4M3FN code (1 sign bit, 4 exponent bits with bias 7, 3
-// mantissa bits, subnormals at exponent 0); codes here are finite
-__device__ __forceinline__ float e4m3_value(uint32_t c) {
-  const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
-  const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20))   // (1 + m/8) 2^(e-7)
-                      : (float)m * 0.001953125f;                          // m 2^-9
-  return (c & 0x80u) ? -mag : mag;
-}
-
-// E4M3 codes (RNE, saturating) of the exact quotients y[k] / ds, k = 0..3, in
-// bytes 0..3. inv_lo and inv_hi bracket 1 / ds by 2^-20 on each
-// side (far more than the rounding of the products), so y * inv_lo and
-// y * inv_hi bracket the exact quotient: where their codes agree, no E4M3
-// rounding boundary lies between them and that code is the quotient's; where
-// they differ, the boundary is the midpoint m of the two neighbouring values
-// and the sign of y - m ds (exact in one FMA) decides, a tie going to the
-// even code, as round-to-nearest-even of the exact quotient does.
-__device__ __forceinline__ uint32_t tie_fix(uint32_t out, uint32_t clo, uint32_t chi, int k,
-                                            float y, float ds) {
-  const uint32_t a = (clo >> (8 * k)) & 0xFFu, b = (chi >> (8 * k)) & 0xFFu;
-  if (a == b) return out;
-  const float va = e4m3_value(a), vb = e4m3_value(b);
-  const float mid = 0.5f * (va + vb);            // exact: neighbours of the format
-  const float res = fmaf(-mid, ds, y);          // sign of y - mid * ds, exact
-  const uint32_t up = va > vb ? a : b, dn = va > vb ? b : a;
-  const uint32_t pick = res > 0.f ? up : res < 0.f ? dn : ((a & 1u) ? b : a);
-  return (out & ~(0xFFu << (8 * k))) | (pick << (8 * k));
-}
-__device__ __forceinline__ uint32_t quant4_exact(float y0, float y1, float y2, float y3,
-                                                 float inv_lo, float inv_hi, float ds) {
-  const uint32_t clo = ptx::pack_e4m3x4(y0 * inv_lo, y1 * inv_lo, y2 * inv_lo, y3 * inv_lo);
-  const uint32_t chi = ptx::pack_e4m3x4(y0 * inv_hi, y1 * inv_hi, y2 * inv_hi, y3 * inv_hi);
-  if (clo == chi) return clo;
-  uint32_t out = clo;
-  out = tie_fix(out, clo, chi, 0, y0, ds);
-  out = tie_fix(out, clo, chi, 1, y1, ds);
-  out = tie_fix(out, clo, chi, 2, y2, ds);
-  out = tie_fix(out, clo, chi, 3, y3, ds);
-  return out;
 }
 
 // ring depth and CTAs per SM of the prep kernel
@@ -337,36 +296,50 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
       if (threadIdx.x == 0) atomicMax(reinterpret_cast<unsigned int*>(tensor_amax), __float_as_uint(bmax));
       continue;
     }
-    // codes are E4M3(y / descale). Without the transform or rotation (y = x
-    // exactly) the code of the exact quotient is taken (quant4_exact); with
-    // them, y itself carries float32 rounding and codes are y * (448 / amax),
-    // the reciprocal taken once per block (times 1 / sqrt(d) with the
-    // transform)
+    // codes are E4M3(y / descale), descale = amax / 448 rounded to float32.
+    // Without the transform or rotation y is the bfloat16 input itself, and
+    // the code of the exact quotient is reached with one product per value:
+    // with x and amax bfloat16, x * 448 / amax is either exactly an E4M3
+    // rounding midpoint or at least 2^-13 (relative) away from every one, and
+    // x / descale differs from it by the descale's own rounding only. So the
+    // reciprocal is nudged by 4 ulps (about 2^-21, far above the rounding of
+    // the product) to the side where the descale's rounding puts the exact
+    // quotient: a midpoint then rounds the way the exact quotient does, and
+    // no other value changes its code. When the descale is exact, ties must
+    // go to even: a reciprocal that is exact too keeps them on the midpoint,
+    // else the block divides (IEEE, rounded once). With the transform or
+    // rotation y carries float32 rounding already and the codes are y *
+    // (448 / amax), the reciprocal taken once per block (times 1 / sqrt(d)
+    // with the transform).
     float inv_ds = bmax > 0.f ? __fdiv_rn(448.0f, bmax) : 1.0f;
-    if (signs) inv_ds *= inv_sqrt_d;
     const float ds = bmax > 0.f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
+    bool divide = false;
+    if (!ROPE && !signs && bmax > 0.f) {
+      const float dd = fmaf(ds, 448.0f, -bmax);   // sign of descale * 448 - amax, exact
+      if (dd > 0.f) inv_ds = __uint_as_float(__float_as_uint(inv_ds) - 4u);
+      else if (dd < 0.f) inv_ds = __uint_as_float(__float_as_uint(inv_ds) + 4u);
+      else divide = fmaf(inv_ds, ds, -1.0f) != 0.f;
+    }
+    if (signs) inv_ds *= inv_sqrt_d;
     if constexpr (MODE == kPrepBlock) {
       if (threadIdx.x == 0) descale[((long long)b * H + h) * nb + blk] = ds;
     }
-    const bool exact = !ROPE && !signs;
-    const float inv_lo = inv_ds * (1.0f - 9.5367431640625e-07f);   // 1 -+ 2^-20
-    const float inv_hi = inv_ds * (1.0f + 9.5367431640625e-07f);
 
 #pragma unroll
     for (int i = 0; i < ITERS; ++i) {
       const int n = row_of(i);
       const int nl = n - blk * 128;
       uint32_t c4[VEC / 4];
-      if (exact) {
-#pragma unroll
-        for (int q = 0; q < VEC / 4; ++q)
-          c4[q] = quant4_exact(y[i][4 * q], y[i][4 * q + 1], y[i][4 * q + 2], y[i][4 * q + 3],
-                               inv_lo, inv_hi, ds);
-      } else {
+      if (!divide) {
 #pragma unroll
         for (int q = 0; q < VEC / 4; ++q)
           c4[q] = ptx::pack_e4m3x4(y[i][4 * q] * inv_ds, y[i][4 * q + 1] * inv_ds,
                                    y[i][4 * q + 2] * inv_ds, y[i][4 * q + 3] * inv_ds);
+      } else {
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q)
+          c4[q] = ptx::pack_e4m3x4(__fdiv_rn(y[i][4 * q], ds), __fdiv_rn(y[i][4 * q + 1], ds),
+                                   __fdiv_rn(y[i][4 * q + 2], ds), __fdiv_rn(y[i][4 * q + 3], ds));
       }
       if (!transpose_out) {
         if (n < N) {

@@ -12,7 +12,7 @@ int launch_fwd_instance(const CUtensorMap& q, const CUtensorMap& k, const CUtens
                         const FwdParams& p, int grid, cudaStream_t stream) {
   using C = FwdCfg<D, DT>;
   auto kern = attn_fwd_kernel<D, DT, CAUSAL, SPLIT>;
-  if constexpr (C::REGSPLIT) {
+  if constexpr (C::QST == 2) {
     // the register split inside the kernel must fit in the block's pool,
     // otherwise setmaxnreg.inc would wait forever: refuse to launch instead
     cudaFuncAttributes fa;
