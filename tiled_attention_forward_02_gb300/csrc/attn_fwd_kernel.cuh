@@ -264,11 +264,16 @@ struct Ctl {
 // spinning, so they do not take issue slots from the warps doing the work
 constexpr uint32_t kWaitSuspendNs = 200000;
 
+// SPIN: poll without the suspend hint, for a warp whose next work depends on
+// nothing else (waking a suspended warp adds latency to its chain)
+template <bool SPIN = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) return true;
+    if (SPIN ? ptx::mbar_try_wait(bar, parity)
+             : ptx::mbar_try_wait_sleep(bar, parity, kWaitSuspendNs))
+      return true;
     if (*ctl.abort_flag) return false;
     if (clock64() - t0 > kWaitBudgetCycles) {
       *ctl.abort_flag = 1;
@@ -280,8 +285,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
 
 // a whole warp waits; the outcome is made warp-uniform so that the
 // warp-collective tcgen05 loads/stores that follow stay convergent
+template <bool SPIN = false>
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
-  const bool ok = wait_bar(bar, parity, ctl);
+  const bool ok = wait_bar<SPIN>(bar, parity, ctl);
   return __all_sync(0xffffffffu, ok);
 }
 

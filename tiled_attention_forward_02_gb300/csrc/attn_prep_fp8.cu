@@ -307,7 +307,9 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     // quotient: a midpoint then rounds the way the exact quotient does, and
     // no other value changes its code. When the descale is exact, ties must
     // go to even: a reciprocal that is exact too keeps them on the midpoint,
-    // else the block divides (IEEE, rounded once). With the transform or
+    // else one correction step q + (x - q * descale) / descale (the residual
+    // is exact in one FMA) lands exactly on a midpoint that the quotient
+    // equals and within an ulp elsewhere. With the transform or
     // rotation y carries float32 rounding already and the codes are y *
     // (448 / amax), the reciprocal taken once per block (times 1 / sqrt(d)
     // with the transform).
@@ -336,10 +338,15 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
           c4[q] = ptx::pack_e4m3x4(y[i][4 * q] * inv_ds, y[i][4 * q + 1] * inv_ds,
                                    y[i][4 * q + 2] * inv_ds, y[i][4 * q + 3] * inv_ds);
       } else {
+        auto quot = [&](float x) {
+          const float q0 = x * inv_ds;
+          const float res = fmaf(-q0, ds, x);
+          return res == 0.f ? q0 : fmaf(res, inv_ds, q0);   // (keeps the sign of a zero)
+        };
 #pragma unroll
         for (int q = 0; q < VEC / 4; ++q)
-          c4[q] = ptx::pack_e4m3x4(__fdiv_rn(y[i][4 * q], ds), __fdiv_rn(y[i][4 * q + 1], ds),
-                                   __fdiv_rn(y[i][4 * q + 2], ds), __fdiv_rn(y[i][4 * q + 3], ds));
+          c4[q] = ptx::pack_e4m3x4(quot(y[i][4 * q]), quot(y[i][4 * q + 1]),
+                                   quot(y[i][4 * q + 2]), quot(y[i][4 * q + 3]));
       }
       if (!transpose_out) {
         if (n < N) {
