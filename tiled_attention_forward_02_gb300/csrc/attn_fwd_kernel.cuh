@@ -264,16 +264,11 @@ struct Ctl {
 // spinning, so they do not take issue slots from the warps doing the work
 constexpr uint32_t kWaitSuspendNs = 200000;
 
-// SPIN: poll without the suspend hint, for a warp whose next work depends on
-// nothing else (waking a suspended warp adds latency to its chain)
-template <bool SPIN = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (SPIN ? ptx::mbar_try_wait(bar, parity)
-             : ptx::mbar_try_wait_sleep(bar, parity, kWaitSuspendNs))
-      return true;
+    if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) return true;
     if (*ctl.abort_flag) return false;
     if (clock64() - t0 > kWaitBudgetCycles) {
       *ctl.abort_flag = 1;
@@ -285,9 +280,30 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
 
 // a whole warp waits; the outcome is made warp-uniform so that the
 // warp-collective tcgen05 loads/stores that follow stay convergent
-template <bool SPIN = false>
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
-  const bool ok = wait_bar<SPIN>(bar, parity, ctl);
+  const bool ok = wait_bar(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// The softmax warps' wait for S: polled without the suspend hint and without
+// reading the abort flag inside the loop (measured: waking a suspended warp,
+// or the extra poll, costs 2-4 % of the forward's time on this wait, which
+// sits on the softmax's critical path). Still bounded by the cycle budget; on
+// expiry it flags the timeout like wait_bar. After another role aborted, it
+// gives up when its own budget runs out.
+__device__ __forceinline__ bool warp_spin_wait_bar(uint32_t bar, uint32_t parity, const Ctl& ctl) {
+  bool ok = true;
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      ok = false;
+      break;
+    }
+  }
+  if (!ok) {
+    *ctl.abort_flag = 1;
+    atomicOr(ctl.status, kStatusTimeout);
+  }
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -898,7 +914,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         }
       }
       for (int j = 0; j < ns; ++j) {
-        ok = warp_wait_bar(bar(B_SFULL + s), s_cnt & 1, ctl);
+        ok = warp_spin_wait_bar(bar(B_SFULL + s), s_cnt & 1, ctl);
         ++s_cnt;
         if (!ok) break;
         ptx::tc_fence_after();
