@@ -247,12 +247,19 @@ class OracleSampler:
         return time.perf_counter() - t0
 
     def rows_for(self, seconds):
-        """Rows that take about `seconds` (fixed cost of a call included)."""
-        small, big = self.rows(self.threads), self.rows(self.threads * 8)
-        t_small, t_big = self.run(small), self.run(big)
-        per_row = max((t_big - t_small) / (len(big) - len(small)), 1e-7)
-        fixed = max(t_small - per_row * len(small), 0.0)
-        return max(self.threads, int((seconds - fixed) / per_row))
+        """Rows that take about `seconds`: after one warm-up call (the first
+        call also pages in the decoded keys and values), the sample doubles
+        until one call takes at least 0.25 s, and the count scales linearly
+        from that call (its fixed cost included, so the estimate errs short).
+        Bounded: at most 48 times the calibrated sample."""
+        self.run(self.rows(self.threads))
+        n = self.threads * 4
+        while True:
+            t = self.run(self.rows(n))
+            if t >= 0.25 or n >= (1 << 22):
+                break
+            n *= 2
+        return max(self.threads, min(int(n * seconds / max(t, 1e-3)), 48 * n))
 
 
 def time_oracle(workload, budget_s=12.0):
