@@ -1003,15 +1003,6 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         const float nbias = bias_extra - mi;
         float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
         const uint32_t prow = prow0 + (uint32_t)(p_cnt & 1) * C::PBYTES;   // shared-memory P
-        // shared-memory P with a moved reference: O_s is rescaled in 32-column
-        // chunks interleaved with the P chunks (O and P both have 128
-        // columns): the TMEM load of O chunk k is issued once P chunk k is
-        // stored (its registers are free), and completes while P chunk k + 1
-        // is computed; O_s holds every previous PV product once PV number
-        // p_cnt - 1 is done
-        static_assert(!C::PSMEM || D == 128, "O chunks paired with P chunks");
-        uint32_t ob[32];
-        bool resc = false;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -1038,20 +1029,6 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
               // (K-major, 128-byte swizzle: chunk c of row r sits at c ^ (r % 8))
               ptx::st_shared_v4(prow + (((2 * k) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
               ptx::st_shared_v4(prow + (((2 * k + 1) ^ (r & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
-              if (any_rescale) {
-                if (k == 0) {
-                  const int n = p_cnt - 1;
-                  ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
-                  if (ok) ptx::tc_fence_after();
-                  resc = ok;
-                } else if (resc) {
-                  ptx::tmem_ld_wait_x32(ob);
-#pragma unroll
-                  for (int c = 0; c < 32; ++c) ob[c] = __float_as_uint(__uint_as_float(ob[c]) * alpha);
-                  ptx::tmem_st_x32(tO + 32 * (k - 1), ob);
-                }
-                if (resc) ptx::tmem_ld_x32_nowait(tO + 32 * k, ob);
-              }
             } else {
               ptx::tmem_st_x8(tS + 8 * k, pk);
             }
@@ -1068,13 +1045,38 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         }
         li += ((sum0 + sum1) + (sum2 + sum3)) * sum_scale;
         if constexpr (C::PSMEM) {
-          if (resc) {   // the last O chunk
-            ptx::tmem_ld_wait_x32(ob);
+          if (any_rescale) {
+            // P is already relative to the moved reference; O_s holds every
+            // previous PV product once PV number p_cnt - 1 is done (it had the
+            // whole exponential phase to finish). The S registers are dead:
+            // O is read 64 columns at a time with both loads in flight.
+            const int n = p_cnt - 1;
+            ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            static_assert(D % 128 == 0, "O rescale in pairs of 64-column loads");
+#pragma unroll 1
+            for (int cb = 0; cb < D; cb += 128) {
+              uint32_t oa[64], ob[64];
+              ptx::tmem_ld_x64_nowait(tO + cb, oa);
+              ptx::tmem_ld_x64_nowait(tO + cb + 64, ob);
+              ptx::tmem_ld_wait_x64x2(oa, ob);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ob[c] = __float_as_uint(__uint_as_float(ob[c]) * alpha);
-            ptx::tmem_st_x32(tO + 96, ob);
+              for (int c = 0; c < 64; c += 2) {
+                float a0, a1, b0, b1;
+                ptx::fma2(a0, a1, __uint_as_float(oa[c]), __uint_as_float(oa[c + 1]), alpha, alpha,
+                          0.f, 0.f);
+                ptx::fma2(b0, b1, __uint_as_float(ob[c]), __uint_as_float(ob[c + 1]), alpha, alpha,
+                          0.f, 0.f);
+                oa[c] = __float_as_uint(a0);
+                oa[c + 1] = __float_as_uint(a1);
+                ob[c] = __float_as_uint(b0);
+                ob[c + 1] = __float_as_uint(b1);
+              }
+              ptx::tmem_st_x64(tO + cb, oa);
+              ptx::tmem_st_x64(tO + cb + 64, ob);
+            }
           }
-          if (!ok) break;
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
