@@ -115,7 +115,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *            in float32 and scaled by r = 448 / amax (float32, once per
  *            block) times 1 / sqrt(d): a code may then differ by one step
  *            where y / descale lies within float32 rounding of a midpoint.
- *   signs    NULL (no transform) or [sign_heads, d] int8 of +1/-1 (device).
+ *   signs    NULL (no transform) or [sign_heads, d] int8 of +1/-1 (device,
+ *            8-byte aligned).
  *            With signs, every row is replaced, before quantisation, by
  *            y = (x * sigma) H_d / sqrt(d) in float32, H_d the Sylvester
  *            Hadamard matrix and sigma the row of head h / (H / sign_heads).

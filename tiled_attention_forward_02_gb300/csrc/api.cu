@@ -284,6 +284,7 @@ int check_prep(const void* x, const void* x8, const float* descale, int B, int H
   if (B == 0 || N == 0) return ATTN_OK;
   if (!x || !x8 || !descale) return ATTN_ERR_INVALID_ARG;
   if (!aligned(x, 128) || !aligned(x8, 128) || !aligned(descale, 16)) return ATTN_ERR_MISALIGNED;
+  if (signs && !aligned(signs, 8)) return ATTN_ERR_MISALIGNED;
   return ATTN_OK;
 }
 }  // namespace

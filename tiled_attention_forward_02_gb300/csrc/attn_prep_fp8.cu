@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   uint8_t* s_t = smem + NS * PC::TILE_BYTES;                   // transposed codes
   uint8_t* tail = s_t + (transpose_out ? D * 128 : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(tail);          // [NS] tile landed
-  float* s_amax = reinterpret_cast<float*>(tail + 8 * NS);     // [8]
+  float* s_amax = reinterpret_cast<float*>(tail + 8 * NS);     // [2][8]
   auto bar = [&](int i) { return ptx::smem_addr(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,27 +166,25 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
       while (!(ok = ptx::mbar_try_wait_sleep(bar(st), (uint32_t)((k / NS) & 1), 100000)))
         if (clock64() - t0 > kPrepWaitCycles) break;
     }
-    if (__syncthreads_or(!ok)) {
-      if (threadIdx.x == 0) {
-        atomicOr(status, 1u);
-        // wait (bounded) for the copies this CTA still has in flight
-        for (long long kk = k; kk < k + NS; ++kk) {
-          if (blockIdx.x + kk * G >= n_tiles) break;
-          const long long t0 = clock64();
-          while (!ptx::mbar_try_wait(bar((int)(kk % NS)), (uint32_t)((kk / NS) & 1)))
-            if (clock64() - t0 > kPrepWaitCycles) break;
-        }
-      }
-      return;
-    }
+    // (a thread whose wait gave up reads stale data; the block leaves at the
+    // amax barrier below, before anything is stored)
     // row of iteration i within the tile: warp*16 + RPW*i + rsub
     auto row_of = [&](int i) { return blk * 128 + warp * 16 + RPW * i + rsub; };
     const uint32_t tile = sbase + st * PC::TILE_BYTES;
 
+    // signs of this lane's channels: chunk j is 8 consecutive channels, one
+    // 8-byte load (the host requires 8-byte aligned signs)
     float sg[VEC];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v)
-      sg[v] = signs ? (float)signs[(long long)(h / sign_group) * D + chan(v)] : 1.f;
+    for (int j = 0; j < CH; ++j) {
+      uint2 w = make_uint2(0x01010101u, 0x01010101u);
+      if (signs)
+        w = __ldg(reinterpret_cast<const uint2*>(signs + (long long)(h / sign_group) * D +
+                                                 8 * (hl + LPR * j)));
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        sg[8 * j + t] = (float)(int8_t)(((t < 4 ? w.x : w.y) >> (8 * (t & 3))) & 0xFFu);
+    }
 
     float y[ITERS][VEC];
     // the whole tile from shared memory (rows past N were zero-filled by the copy)
@@ -196,8 +194,6 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
       for (int j = 0; j < CH; ++j)
         load_chunk(tile + (uint32_t)((warp * 16 + RPW * i + rsub) * D * 2 + (hl + LPR * j) * 16),
                    &y[i][8 * j]);
-    __syncthreads();   // stage st is free: refill it with the tile NS ahead
-    if (threadIdx.x == 0) issue(k + NS);
 
     float amax = 0.f;
 #pragma unroll
@@ -279,16 +275,36 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     // that of the scaled values, y is scaled together with the quantisation
     const float inv_sqrt_d =
         !signs ? 1.f : (D == 64) ? 0.125f : (D == 128) ? 0.08838834764831845f : 0.0625f;
+    // one barrier per tile: it gathers the block amax (slots alternate by
+    // tile parity, so a warp one tile ahead cannot overwrite a slot still
+    // being read), makes the abort decision uniform, and frees the stage
+    // (every row is in registers once all threads reached it)
+    float* amax_slot = s_amax + 8 * (int)(k & 1);
+    if constexpr (MODE != kPrepTensor) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (lane == 0) amax_slot[warp] = amax;
+    }
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        atomicOr(status, 1u);
+        // wait (bounded) for the copies this CTA still has in flight
+        for (long long kk = k; kk < k + NS; ++kk) {
+          if (blockIdx.x + kk * G >= n_tiles) break;
+          const long long t0 = clock64();
+          while (!ptx::mbar_try_wait(bar((int)(kk % NS)), (uint32_t)((kk / NS) & 1)))
+            if (clock64() - t0 > kPrepWaitCycles) break;
+        }
+      }
+      return;
+    }
+    if (threadIdx.x == 0) issue(k + NS);   // stage st is free: the tile NS ahead
     if constexpr (MODE == kPrepTensor) {
       bmax = *tensor_amax;   // written by the amax pass, read-only here
     } else {
+      bmax = amax_slot[0];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      if (lane == 0) s_amax[warp] = amax;
-      __syncthreads();
-      bmax = s_amax[0];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, s_amax[w]);
+      for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, amax_slot[w]);
       if (signs) bmax *= inv_sqrt_d;
     }
     if constexpr (MODE == kPrepTensorAmax) {
