@@ -195,6 +195,31 @@ int attn_prep_fp8_rope(const void* x, void* x8, float* descale, int B, int H, in
                        int sign_heads, void* stream);
 
 /*
+ * attn_prep_fp8_qkv - the FP8 preparation of one attention call in one
+ * launch: Q and K as attn_prep_fp8 (per-block codes, BSHD) or, with rotary
+ * tables, as attn_prep_fp8_rope; V as attn_prep_fp8 with transpose_out = 1.
+ * The results are those of the three separate calls, bit for bit; one
+ * launch pays the ramp-up and tail of a persistent kernel once instead of
+ * three times.  This entry point is an addition of this library, not a step
+ * of the pages' method.
+ *
+ *   q [B, Nq, Hq, d], k, v [B, Nk, Hkv, d]  bfloat16 (read)
+ *   q8 [B, Nq, Hq, d], k8 [B, Nk, Hkv, d]   E4M3 codes (written)
+ *   v8t [B, Hkv, d, Nkpad]                   E4M3 codes, Nkpad = Nk rounded up to 16
+ *   q_descale [B, Hq, ceil(Nq/128)], k_descale, v_descale [B, Hkv, ceil(Nk/128)]
+ *   signs     NULL or [Hkv, d] int8 +1/-1 (8-byte aligned): Q and K take the
+ *             transform, query head h using row h / (Hq / Hkv)
+ *   rope_cos, rope_sin  both NULL or both [max(Nq, Nk), d/2] float32
+ *             (attn_rope_table, 16-byte aligned): Q and K are rotated first
+ *   d         64, 128 or 256
+ * Returns as attn_prep_fp8.
+ */
+int attn_prep_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8t,
+                      float* q_descale, float* k_descale, float* v_descale, int B, int Hq,
+                      int Hkv, int64_t Nq, int64_t Nk, int d, const int8_t* signs,
+                      const float* rope_cos, const float* rope_sin, void* stream);
+
+/*
  * attn_fwd_fp8 - fused attention forward on FP8 E4M3 inputs.
  *
  *   q8        [B, Nq, Hq, d]     E4M3 codes       q_descale [B, Hq, ceil(Nq/128)]

@@ -424,3 +424,37 @@ def test_prep_rope_hadamard_full_size_sampled(gpu_lib):
     q_exact = y / ods.astype(np.float64)[rows[:, 0], rows[:, 1], rows[:, 2] // 128][:, None]
     g = codes.cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]]
     _codes_near(g, q_exact)
+
+
+# --- Q, K, V prepared in one launch ------------------------------------------
+
+@pytest.mark.parametrize("variant", ["plain", "hadamard", "rope_hadamard"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_prep_qkv_one_launch_equals_separate_calls(gpu_lib, variant, d):
+    """attn_prep_fp8_qkv gives the codes and descales of the three separate
+    calls bit for bit (GQA, Nq != Nk, ragged last blocks); without the
+    transform they are also the oracle's."""
+    B, Nq, Nk, Hq, Hkv = 2, 650, 390, 4, 2
+    q, k, v = synth.attn_inputs(B, Nq, Nk, Hq, Hkv, d, dtype=torch.bfloat16, seed=25,
+                                outlier_frac=1e-3, device="cuda")
+    signs = _signs(Hkv, d) if variant != "plain" else None
+    rope = gpu_lib.attn_rope_table(max(Nq, Nk), d) if variant == "rope_hadamard" else None
+    got = gpu_lib.attn_prep_fp8_qkv(q, k, v, signs=signs, rope=rope)
+    assert gpu_lib.get_status() == 0
+    if rope is None:
+        want = (*gpu_lib.attn_prep_fp8(q, signs=signs, sign_heads=Hkv),
+                *gpu_lib.attn_prep_fp8(k, signs=signs, sign_heads=Hkv),
+                *gpu_lib.attn_prep_fp8(v, transpose_out=True))
+    else:
+        cq, sq = gpu_lib.attn_rope_table(Nq, d)
+        ck, sk = gpu_lib.attn_rope_table(Nk, d)
+        want = (*gpu_lib.attn_prep_fp8_rope(q, cq, sq, signs=signs, sign_heads=Hkv),
+                *gpu_lib.attn_prep_fp8_rope(k, ck, sk, signs=signs, sign_heads=Hkv),
+                *gpu_lib.attn_prep_fp8(v, transpose_out=True))
+    for g, w in zip(got, want):
+        assert g.shape == w.shape and torch.equal(g, w)
+    if variant == "plain":
+        for t, (c, ds) in zip((q, k), ((got[0], got[1]), (got[2], got[3]))):
+            oc, ods, _ = ofp8.prepare(t.float().cpu().numpy(), None, False)
+            np.testing.assert_array_equal(c.cpu().numpy(), oc)
+            np.testing.assert_array_equal(ds.cpu().numpy(), ods)

@@ -26,7 +26,8 @@ ERR_SCRATCH = -7
 EXPORTS = ("attn_fwd", "attn_prep_fp8", "attn_fwd_fp8", "attn_get_status", "attn_strerror",
            "attn_launch_count", "attn_fwd_splitkv", "attn_splitkv_workspace_bytes",
            "attn_splitkv_default_splits", "attn_fwd_splitkv_noalloc", "attn_prep_fp8_per_tensor",
-           "attn_rope_table", "attn_prep_fp8_rope", "attn_selftest_bounded_wait")
+           "attn_rope_table", "attn_prep_fp8_rope", "attn_selftest_bounded_wait",
+           "attn_prep_fp8_qkv")
 
 _lib = None
 
@@ -76,6 +77,9 @@ def load():
     lib.attn_prep_fp8_per_tensor.argtypes = [vp, vp, vp, i32, i32, i64, i32, vp, i32, i32, vp]
     lib.attn_rope_table.restype = i32
     lib.attn_rope_table.argtypes = [vp, vp, i64, i32, ctypes.c_double, i64, vp]
+    lib.attn_prep_fp8_qkv.restype = i32
+    lib.attn_prep_fp8_qkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i64, i64,
+                                      i32, vp, vp, vp, vp]
     lib.attn_prep_fp8_rope.restype = i32
     lib.attn_prep_fp8_rope.argtypes = [vp, vp, vp, i32, i32, i64, i32, vp, vp, vp, i32, vp]
     _lib = lib
@@ -231,6 +235,42 @@ def attn_prep_fp8(x, signs=None, sign_heads: int | None = None, transpose_out: b
                               int(bool(transpose_out)), _stream(stream))
     _check(rc, "attn_prep_fp8")
     return out, descale
+
+
+def attn_prep_fp8_qkv(q, k, v, signs=None, rope=None, out=None, stream=None):
+    """The FP8 preparation of one attention call in one launch: Q and K per
+    block (with the transform when ``signs`` [Hkv, d] is given, rotated first
+    when ``rope`` = (cos, sin) from attn_rope_table covering max(Nq, Nk)
+    positions), V transposed.  Returns (q8, qd, k8, kd, v8t, vd), the same as
+    the separate attn_prep_fp8 / attn_prep_fp8_rope calls.  ``out`` may hold
+    those six tensors to be written in place."""
+    _need_cuda(q, k, v)
+    if q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must be bfloat16")
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    if v.shape != k.shape:
+        raise ValueError("k and v must have the same shape")
+    if out is None:
+        dev = q.device
+        npad = (Nk + 15) // 16 * 16
+        out = (torch.empty(q.shape, dtype=torch.uint8, device=dev),
+               torch.empty((B, Hq, (Nq + 127) // 128), dtype=torch.float32, device=dev),
+               torch.empty(k.shape, dtype=torch.uint8, device=dev),
+               torch.empty((B, Hkv, (Nk + 127) // 128), dtype=torch.float32, device=dev),
+               torch.empty((B, Hkv, d, npad), dtype=torch.uint8, device=dev),
+               torch.empty((B, Hkv, (Nk + 127) // 128), dtype=torch.float32, device=dev))
+    q8, qd, k8, kd, v8, vd = out
+    if signs is not None:
+        _need_cuda(signs)
+        if signs.dtype != torch.int8 or tuple(signs.shape) != (Hkv, d):
+            raise ValueError("signs must be int8 [Hkv, d]")
+    cos, sin = (None, None) if rope is None else rope
+    rc = load().attn_prep_fp8_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(k8), _ptr(v8),
+                                  _ptr(qd), _ptr(kd), _ptr(vd), B, Hq, Hkv, Nq, Nk, d,
+                                  _ptr(signs), _ptr(cos), _ptr(sin), _stream(stream))
+    _check(rc, "attn_prep_fp8_qkv")
+    return q8, qd, k8, kd, v8, vd
 
 
 def attn_prep_fp8_per_tensor(x, signs=None, sign_heads: int | None = None,

@@ -317,6 +317,48 @@ extern "C" int attn_prep_fp8_per_tensor(const void* x, void* x8, float* descale,
                          nullptr, 1, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int attn_prep_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8,
+                                 void* v8t, float* q_descale, float* k_descale, float* v_descale,
+                                 int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d,
+                                 const int8_t* signs, const float* rope_cos, const float* rope_sin,
+                                 void* stream) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if ((rope_cos == nullptr) != (rope_sin == nullptr)) return ATTN_ERR_INVALID_ARG;
+  int rc;
+  if ((rc = check_prep(q, q8, q_descale, B, Hq, Nq, d, signs, Hkv, 0)) ||
+      (rc = check_prep(k, k8, k_descale, B, Hkv, Nk, d, signs, Hkv, 0)) ||
+      (rc = check_prep(v, v8t, v_descale, B, Hkv, Nk, d, nullptr, 1, 1)))
+    return rc;
+  if (rope_cos && (!aligned(rope_cos, 16) || !aligned(rope_sin, 16))) return ATTN_ERR_MISALIGNED;
+  if (B == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != ATTN_OK) return rc;
+  // Q, K, V as three tensors of one launch (Q and K: per-block codes with the
+  // optional rotation and transform; V: transposed codes)
+  PrepJobs J{};
+  int n = 0;
+  long long tiles = 0;
+  auto add = [&](const void* x, void* x8, float* ds, int H, int64_t N, const int8_t* sg,
+                 int group, int tr, bool rot) -> int {
+    if (N == 0) return ATTN_OK;
+    const int r = map_prep(&J.map[n], x, B, N, H, d);
+    if (r != ATTN_OK) return r;
+    J.job[n] = prep_job(x8, ds, B, H, (int)N, sg, group, tr, rot ? rope_cos : nullptr,
+                        rot ? rope_sin : nullptr, tiles);
+    tiles += (long long)B * J.job[n].nb * H;
+    ++n;
+    return ATTN_OK;
+  };
+  if ((rc = add(q, q8, q_descale, Hq, Nq, signs, Hq / Hkv, 0, true)) ||
+      (rc = add(k, k8, k_descale, Hkv, Nk, signs, 1, 0, true)) ||
+      (rc = add(v, v8t, v_descale, Hkv, Nk, nullptr, 1, 1, false)))
+    return rc;
+  J.n_jobs = n;
+  J.any_transpose = Nk > 0 ? 1 : 0;
+  J.n_tiles = tiles;
+  return launch_prep_jobs(J, d, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int attn_rope_table(float* rope_cos, float* rope_sin, int64_t N, int d, double base,
                                int64_t pos0, void* stream) {
   if (N < 0 || N > kMaxRows || d < 2 || d > 256 || (d & 1)) return ATTN_ERR_INVALID_ARG;

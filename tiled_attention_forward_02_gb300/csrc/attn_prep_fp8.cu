@@ -77,21 +77,6 @@ struct PrepCfg {
 
 constexpr long long kPrepWaitCycles = 4000000000LL;   // about 2 s
 
-// arguments of one prep launch
-struct PrepLaunch {
-  const CUtensorMap* map;   // x as (d, H, N, B), box d x 1 x 128 x 1, no swizzle
-  uint8_t* x8;
-  float* descale;
-  const int8_t* signs;
-  int sign_group;
-  int B, H, N, nb, Npad;
-  const float* rope_cos;
-  const float* rope_sin;
-  float* tensor_amax;
-  int sm_count;
-  unsigned int* status;
-  cudaStream_t stream;
-};
 
 // quantisation modes
 enum PrepMode : int {
@@ -100,13 +85,12 @@ enum PrepMode : int {
   kPrepTensor = 2,      // per-tensor, second pass: codes from the tensor amax
 };
 
+// A launch walks the tiles of up to three tensors (Q, K, V of one attention
+// call) one tensor after the other, so that the ramp-up and the tail of a
+// persistent launch (about 7 us) are paid once per step instead of per tensor.
 template <int D, int MODE, bool ROPE>
 __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
-    prep_fp8_kernel(const __grid_constant__ CUtensorMap tmX, uint8_t* __restrict__ x8,
-                    float* __restrict__ descale, const int8_t* __restrict__ signs,
-                    int sign_group, int B, int H, int N, int nb, int Npad, int transpose_out,
-                    const float* __restrict__ rope_cos, const float* __restrict__ rope_sin,
-                    float* tensor_amax, unsigned int* status) {
+    prep_fp8_kernel(const __grid_constant__ PrepJobs J, float* tensor_amax, unsigned int* status) {
   using PC = PrepCfg<D>;
   constexpr int LPR = PC::LPR;        // lanes per row
   constexpr int CH = PC::CH;          // chunks of 8 channels per lane
@@ -120,7 +104,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = sraw + pad;                           // NS tiles
   uint8_t* s_t = smem + NS * PC::TILE_BYTES;                   // transposed codes
-  uint8_t* tail = s_t + (transpose_out ? D * 128 : 0);
+  uint8_t* tail = s_t + (J.any_transpose ? D * 128 : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(tail);          // [NS] tile landed
   float* s_amax = reinterpret_cast<float*>(tail + 8 * NS);     // [2][8]
   auto bar = [&](int i) { return ptx::smem_addr(&bars[i]); };
@@ -129,25 +113,36 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   const int rsub = lane / LPR, hl = lane % LPR;
   // channel of value v = 8 j + t of this lane: 8 (hl + LPR j) + t
   auto chan = [&](int v) { return 8 * (hl + LPR * (v >> 3)) + (v & 7); };
-  const long long n_tiles = (long long)B * nb * H;
+  const long long n_tiles = J.n_tiles;
   const long long G = gridDim.x;
+  // tensor of tile t, its parameters and its tensor map (constant indices
+  // into the kernel parameter)
+  auto job_of = [&](long long t) {
+    return (J.n_jobs > 1 && t >= J.job[1].tile0 ? 1 : 0) +
+           (J.n_jobs > 2 && t >= J.job[2].tile0 ? 1 : 0);
+  };
+  auto job = [&](int jj) { return jj == 0 ? J.job[0] : jj == 1 ? J.job[1] : J.job[2]; };
+  auto map_of = [&](int jj) { return jj == 0 ? &J.map[0] : jj == 1 ? &J.map[1] : &J.map[2]; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) ptx::mbar_init(bar(i), 1);
     ptx::fence_barrier_init();
-    ptx::tma_prefetch_desc(&tmX);
+    for (int jj = 0; jj < J.n_jobs; ++jj) ptx::tma_prefetch_desc(map_of(jj));
   }
   __syncthreads();
-  // tile t: heads fastest, then blocks, then batch
+  // tile t of a tensor: heads fastest, then blocks, then batch
   auto issue = [&](long long k) {   // copy the CTA's k-th tile into stage k % NS
     const long long t = blockIdx.x + k * G;
     if (t >= n_tiles) return;
-    const int th = (int)(t % H);
-    const long long r = t / H;
-    const int tblk = (int)(r % nb), tb = (int)(r / nb);
+    const int jj = job_of(t);
+    const PrepJob jb = job(jj);
+    const long long tl = t - jb.tile0;
+    const int th = (int)(tl % jb.H);
+    const long long r = tl / jb.H;
+    const int tblk = (int)(r % jb.nb), tb = (int)(r / jb.nb);
     const int st = (int)(k % NS);
     ptx::mbar_arrive_expect_tx(bar(st), PC::TILE_BYTES);
-    ptx::tma_load_4d(sbase + st * PC::TILE_BYTES, &tmX, bar(st), 0, th, tblk * 128, tb);
+    ptx::tma_load_4d(sbase + st * PC::TILE_BYTES, map_of(jj), bar(st), 0, th, tblk * 128, tb);
   };
   if (threadIdx.x == 0)
     for (int k = 0; k < NS; ++k) issue(k);
@@ -155,8 +150,17 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   for (long long k = 0;; ++k) {
     const long long t = blockIdx.x + k * G;
     if (t >= n_tiles) break;
-    const int h = (int)(t % H);
-    const long long rr = t / H;
+    const PrepJob jb = job(job_of(t));
+    const int H = jb.H, N = jb.N, nb = jb.nb, Npad = jb.Npad;
+    const int transpose_out = jb.transpose_out, sign_group = jb.sign_group;
+    uint8_t* __restrict__ x8 = jb.x8;
+    float* __restrict__ descale = jb.descale;
+    const int8_t* __restrict__ signs = jb.signs;
+    const float* __restrict__ rope_cos = jb.rope_cos;
+    const float* __restrict__ rope_sin = jb.rope_sin;
+    const long long tl = t - jb.tile0;
+    const int h = (int)(tl % H);
+    const long long rr = tl / H;
     const int blk = (int)(rr % nb), b = (int)(rr / nb);
     const int st = (int)(k % NS);
     // bounded wait for the tile; every thread takes the same decision
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < ITERS; ++i) {
-      if constexpr (ROPE) {
+      if (ROPE && rope_cos) {
         // (y_c, y_{c+D/2}) -> (y_c cos - y_{c+D/2} sin, y_{c+D/2} cos + y_c sin).
         // With two or more chunks per lane the partner of chunk j is chunk
         // j ^ CH/2 of the same lane; with one (d = 64) it is lane hl ^ LPR/2.
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     float inv_ds = bmax > 0.f ? __fdiv_rn(448.0f, bmax) : 1.0f;
     const float ds = bmax > 0.f ? __fdiv_rn(bmax, 448.0f) : 1.0f;
     bool divide = false;
-    if (!ROPE && !signs && bmax > 0.f) {
+    if (!rope_cos && !signs && bmax > 0.f) {
       const float dd = fmaf(ds, 448.0f, -bmax);   // sign of descale * 448 - amax, exact
       if (dd > 0.f) inv_ds = __uint_as_float(__float_as_uint(inv_ds) - 4u);
       else if (dd < 0.f) inv_ds = __uint_as_float(__float_as_uint(inv_ds) + 4u);
@@ -429,65 +433,78 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float* __restrict__ cos
 }
 
 template <int D, int MODE, bool ROPE>
-int launch_prep_instance(const PrepLaunch& L, int mode_transpose) {
+int launch_prep_instance(const PrepJobs& J, int sm_count, float* tensor_amax,
+                         unsigned int* status, cudaStream_t stream) {
   auto kern = prep_fp8_kernel<D, MODE, ROPE>;
-  const int smem = PrepCfg<D>::smem_bytes(mode_transpose);
+  const int smem = PrepCfg<D>::smem_bytes(J.any_transpose);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prep)");
-  const long long tiles = (long long)L.B * L.nb * L.H;
-  const long long cap = (long long)PrepCfg<D>::CTAS_PER_SM * L.sm_count;
-  const int grid = (int)(tiles < cap ? tiles : cap);
-  kern<<<grid, 256, smem, L.stream>>>(*L.map, L.x8, L.descale, L.signs, L.sign_group, L.B, L.H,
-                                      L.N, L.nb, L.Npad, mode_transpose, L.rope_cos, L.rope_sin,
-                                      L.tensor_amax, L.status);
+  const long long cap = (long long)PrepCfg<D>::CTAS_PER_SM * sm_count;
+  const int grid = (int)(J.n_tiles < cap ? J.n_tiles : cap);
+  kern<<<grid, 256, smem, stream>>>(J, tensor_amax, status);
   note_launch();
   return check_launch();
 }
 
 template <int MODE, bool ROPE>
-int launch_prep_d(int d, const PrepLaunch& L, int transpose_out) {
+int launch_prep_d(int d, const PrepJobs& J, int sm_count, float* tensor_amax, unsigned int* status,
+                  cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_prep_instance<64, MODE, ROPE>(L, transpose_out);
-    case 128: return launch_prep_instance<128, MODE, ROPE>(L, transpose_out);
-    case 256: return launch_prep_instance<256, MODE, ROPE>(L, transpose_out);
+    case 64: return launch_prep_instance<64, MODE, ROPE>(J, sm_count, tensor_amax, status, stream);
+    case 128: return launch_prep_instance<128, MODE, ROPE>(J, sm_count, tensor_amax, status, stream);
+    case 256: return launch_prep_instance<256, MODE, ROPE>(J, sm_count, tensor_amax, status, stream);
     default: return ATTN_ERR_UNSUPPORTED;
   }
+}
+
+PrepJob prep_job(void* x8, float* descale, int B, int H, int N, const int8_t* signs,
+                 int sign_group, int transpose_out, const float* rope_cos, const float* rope_sin,
+                 long long tile0) {
+  PrepJob jb{};
+  jb.x8 = static_cast<uint8_t*>(x8);
+  jb.descale = descale;
+  jb.signs = signs;
+  jb.sign_group = sign_group;
+  jb.rope_cos = rope_cos;
+  jb.rope_sin = rope_sin;
+  jb.H = H;
+  jb.N = N;
+  jb.nb = (N + 127) / 128;
+  jb.Npad = (N + 15) / 16 * 16;
+  jb.transpose_out = transpose_out;
+  jb.tile0 = tile0;
+  (void)B;
+  return jb;
+}
+
+int launch_prep_jobs(const PrepJobs& J, int d, int sm_count, unsigned int* status,
+                     cudaStream_t stream) {
+  bool rope = false;
+  for (int i = 0; i < J.n_jobs; ++i) rope = rope || J.job[i].rope_cos != nullptr;
+  if (rope) return launch_prep_d<kPrepBlock, true>(d, J, sm_count, nullptr, status, stream);
+  return launch_prep_d<kPrepBlock, false>(d, J, sm_count, nullptr, status, stream);
 }
 
 int launch_prep_fp8(const CUtensorMap& map_x, void* x8, float* descale, int B, int H, int N, int d,
                     const int8_t* signs, int sign_group, int transpose_out, const float* rope_cos,
                     const float* rope_sin, int per_tensor, int sm_count, unsigned int* status,
                     cudaStream_t stream) {
-  PrepLaunch L{};
-  L.map = &map_x;
-  L.x8 = static_cast<uint8_t*>(x8);
-  L.descale = descale;
-  L.signs = signs;
-  L.sign_group = sign_group;
-  L.B = B;
-  L.H = H;
-  L.N = N;
-  L.nb = (N + 127) / 128;
-  L.Npad = (N + 15) / 16 * 16;
-  L.rope_cos = rope_cos;
-  L.rope_sin = rope_sin;
-  L.sm_count = sm_count;
-  L.status = status;
-  L.stream = stream;
-  if (!per_tensor) {
-    if (rope_cos) return launch_prep_d<kPrepBlock, true>(d, L, transpose_out);
-    return launch_prep_d<kPrepBlock, false>(d, L, transpose_out);
-  }
+  PrepJobs J{};
+  J.map[0] = map_x;
+  J.job[0] = prep_job(x8, descale, B, H, N, signs, sign_group, transpose_out, rope_cos, rope_sin, 0);
+  J.n_jobs = 1;
+  J.any_transpose = transpose_out;
+  J.n_tiles = (long long)B * J.job[0].nb * H;
+  if (!per_tensor) return launch_prep_jobs(J, d, sm_count, status, stream);
   if (rope_cos) return ATTN_ERR_UNSUPPORTED;
   // the tensor amax is accumulated in descale[0] and read from there
   cudaError_t e = cudaMemsetAsync(descale, 0, sizeof(float), stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(descale)");
-  L.tensor_amax = descale;
-  int rc = launch_prep_d<kPrepTensorAmax, false>(d, L, 0);
+  int rc = launch_prep_d<kPrepTensorAmax, false>(d, J, sm_count, descale, status, stream);
   if (rc != ATTN_OK) return rc;
-  rc = launch_prep_d<kPrepTensor, false>(d, L, transpose_out);
+  rc = launch_prep_d<kPrepTensor, false>(d, J, sm_count, descale, status, stream);
   if (rc != ATTN_OK) return rc;
-  prep_fill_descale_kernel<<<1, 256, 0, stream>>>(descale, (long long)B * H * L.nb);
+  prep_fill_descale_kernel<<<1, 256, 0, stream>>>(descale, (long long)B * H * J.job[0].nb);
   note_launch();
   return check_launch();
 }

@@ -68,6 +68,35 @@ int launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, fl
                          int n_splits, int B, int Hq, int Nq, int d, int dtype, int sm_count,
                          cudaStream_t stream);
 
+// One tensor of an FP8 prep launch (per-block mode): codes x8 (BSHD, or
+// [B, H, d, Npad] when transpose_out), descales [B, H, nb], optional signs
+// [H / sign_group, d] and rotary tables [N, d/2]; tile0 is its first tile in
+// the launch (tiles of a tensor: heads fastest, then 128-token blocks, then
+// batch).
+struct PrepJob {
+  uint8_t* x8;
+  float* descale;
+  const int8_t* signs;
+  const float* rope_cos;
+  const float* rope_sin;
+  long long tile0;
+  int sign_group, H, N, nb, Npad, transpose_out;
+};
+// up to three tensors in one launch; map[i]: tensor i's bf16 input as
+// (d, H, N, B), box d x 1 x 128 x 1, no swizzle
+struct PrepJobs {
+  CUtensorMap map[3];
+  PrepJob job[3];
+  int n_jobs;
+  int any_transpose;
+  long long n_tiles;
+};
+PrepJob prep_job(void* x8, float* descale, int B, int H, int N, const int8_t* signs,
+                 int sign_group, int transpose_out, const float* rope_cos, const float* rope_sin,
+                 long long tile0);
+int launch_prep_jobs(const PrepJobs& J, int d, int sm_count, unsigned int* status,
+                     cudaStream_t stream);
+
 // per_tensor: one scale for the tensor (descale[0] is used as the amax
 // accumulator, then every block's descale is written); rope_cos / rope_sin:
 // NULL or float32 [N, d/2] tables, rotation before the transform
