@@ -33,7 +33,7 @@
 // Tensor memory (512 columns x 128 lanes, FP32): S_s at column 128 s,
 // O_s at 128 QST + D s.  16-bit P_s (64 columns) is written over the first
 // columns of S_s after S_s has been read. FP8 with two query tiles writes P_s
-// to one of three shared-memory buffers of its tile instead and releases S_s as
+// to one of two shared-memory buffers of its tile instead and releases S_s as
 // soon as it is in registers, so the tile's next S GEMM runs while its softmax
 // still computes P (order per key tile: S_0(j), PV_0(j-1), S_1(j), PV_1(j-1)).
 //
@@ -105,11 +105,7 @@ struct FwdCfg {
   // while the softmax of its current key tile still computes P
   static constexpr bool PSMEM = (DT == DT_E4M3) && (QST == 2);
   static constexpr int PBYTES = BM * BN * ELT;      // one P tile (K-major, 128-byte swizzle)
-  // P buffers per query tile: with three, the softmax writing P number n
-  // needs PV number n - 3 done, a full key tile more slack than with two
-  // (measured: the wait for a free buffer cost 8 % with two)
-  static constexpr int NPBUF = 3;
-  static constexpr int PTOTAL = PSMEM ? QST * NPBUF * PBYTES : 0;
+  static constexpr int PTOTAL = PSMEM ? QST * 2 * PBYTES : 0;   // two buffers per query tile
   static constexpr int SLOT_FIT =
       (SMEM_LIMIT - 1024 - SMEM_TAIL - QST * QBYTES - PTOTAL) / KVBYTES;
   static constexpr int NSLOT = SLOT_FIT > 8 ? 8 : SLOT_FIT;
@@ -365,12 +361,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
   constexpr int B_OFULL = B_PFULL + 2;       // [2]   last PV of unit done    (commit)
   constexpr int B_OEMPTY = B_OFULL + 2;      // [2]   epilogue read O_s       (4 warp arrivals)
   constexpr int B_DRAIN = B_OEMPTY + 2;      // [1]   all MMAs of this CTA done (commit)
-  // shared-memory P only: P buffer b of tile s is entry NPBUF s + b
+  // shared-memory P only: P buffer b of tile s is entry 2 s + b
   constexpr int B_SFREE = B_DRAIN + 1;       // [2]   S_s read into registers (4 warp arrivals)
-  constexpr int NPB = C::NPBUF;
-  constexpr int B_PFULLB = B_SFREE + 2;      // [2xNPB] P buffer written    (4 warp arrivals)
-  constexpr int B_PFREEB = B_PFULLB + 2 * NPB;   // [2xNPB] PV done reading it (commit)
-  constexpr int NBARS = B_PFREEB + 2 * NPB;
+  constexpr int B_PFULLB = B_SFREE + 2;      // [2x2] P buffer written      (4 warp arrivals)
+  constexpr int B_PFREEB = B_PFULLB + 4;     // [2x2] PV done reading it    (commit)
+  constexpr int NBARS = B_PFREEB + 4;
   static_assert(NBARS * 8 + 16 <= C::SMEM_TAIL, "barrier table too large");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -399,7 +394,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     }
     ptx::mbar_init(bar(B_DRAIN), 1);
     for (int s = 0; s < 2; ++s) ptx::mbar_init(bar(B_SFREE + s), 4);
-    for (int i = 0; i < 2 * NPB; ++i) {
+    for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(bar(B_PFULLB + i), 4);
       ptx::mbar_init(bar(B_PFREEB + i), 1);
     }
@@ -510,24 +505,23 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         // until the softmax of tile s holds S_s(j-1) in registers, so it runs
         // while that softmax still computes P_s(j-1); PV reads P from shared
         // memory and its completion frees the buffer. PV number n of a tile
-        // uses buffer n % NPBUF, whose barriers complete once per NPBUF PVs.
+        // uses buffer n % 2, whose barriers complete once per two PVs.
         int kv_it = 0, u_it = 0;
         int pv_cnt[2] = {0, 0};   // PV GEMMs issued per query tile
         int sg_cnt[2] = {0, 0};   // S GEMMs issued per query tile
         bool ok = true;
         const uint32_t qlo0 = sdesc_lo(sQ, 16);
         const uint32_t plo0 = sdesc_lo(sP, 16);   // buffer i at plo0 + i * (PBYTES >> 4)
-        // P buffer b (= n % NPBUF) of tile s
-        auto pv_ss = [&](int s, int b, bool first, uint32_t vlo) {
+        auto pv_ss = [&](int s, int n, bool first, uint32_t vlo) {
           const uint32_t tO = tmem + C::O_COL0 + D * s;
-          const uint32_t plo = plo0 + (uint32_t)(NPB * s + b) * (C::PBYTES >> 4);
+          const uint32_t plo = plo0 + (uint32_t)(2 * s + (n & 1)) * (C::PBYTES >> 4);
           if (first)
             issue_s_mmas<DT, C::CHUNK_BYTES, false>(tO, plo, vlo, idO,
                                                     std::make_index_sequence<C::BN * C::ELT / 32>{});
           else
             issue_s_mmas<DT, C::CHUNK_BYTES, true>(tO, plo, vlo, idO,
                                                    std::make_index_sequence<C::BN * C::ELT / 32>{});
-          ptx::tc_commit(bar(B_PFREEB + NPB * s + b));
+          ptx::tc_commit(bar(B_PFREEB + 2 * s + (n & 1)));
         };
         for (int it = 0; ok; ++it) {
           const int u = unit_of_round<CAUSAL>(it, p);
@@ -549,9 +543,6 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
               uint32_t kph = ((kv_it + 4) / NSLOT) & 1;
               uint32_t sf0 = (sg_cnt[0] - 1) & 1, sf1 = (sg_cnt[1] - 1) & 1;
               int n0 = pv_cnt[0], n1 = pv_cnt[1];
-              // P buffer and phase of PV n0 / n1 as running counters
-              int b0 = n0 % NPB, b1 = n1 % NPB;
-              uint32_t ph0 = (n0 / NPB) & 1, ph1 = (n1 / NPB) & 1;
               const uint32_t tS0 = tmem + C::S_COL0, tS1 = tS0 + 128;
               bool sok = true;
               for (; j < jend; ++j) {
@@ -563,30 +554,22 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                 issue_s(tS0, qlo0, klo);
                 ptx::tc_commit(bar(B_SFULL + 0));
                 sok &= wait_bar(bar(B_KVFULL + vs), vph, ctl);
-                sok &= wait_bar(bar(B_PFULLB + b0), ph0, ctl);
+                sok &= wait_bar(bar(B_PFULLB + (n0 & 1)), (n0 >> 1) & 1, ctl);
                 ptx::tc_fence_after();
-                pv_ss(0, b0, false, vlo);
+                pv_ss(0, n0, false, vlo);
                 sok &= wait_bar(bar(B_SFREE + 1), sf1, ctl);
                 ptx::tc_fence_after();
                 issue_s(tS1, qlo0 + (C::QBYTES >> 4), klo);
                 ptx::tc_commit(bar(B_SFULL + 1));
                 ptx::tc_commit(bar(B_KVEMPTY + ks));
-                sok &= wait_bar(bar(B_PFULLB + NPB + b1), ph1, ctl);
+                sok &= wait_bar(bar(B_PFULLB + 2 + (n1 & 1)), (n1 >> 1) & 1, ctl);
                 ptx::tc_fence_after();
-                pv_ss(1, b1, false, vlo);
+                pv_ss(1, n1, false, vlo);
                 ptx::tc_commit(bar(B_KVEMPTY + vs));
                 sf0 ^= 1u;
                 sf1 ^= 1u;
                 ++n0;
                 ++n1;
-                if (++b0 == NPB) {
-                  b0 = 0;
-                  ph0 ^= 1u;
-                }
-                if (++b1 == NPB) {
-                  b1 = 0;
-                  ph1 ^= 1u;
-                }
                 vs = ks + 1;
                 vph = kph;
                 if (vs == NSLOT) {
@@ -638,11 +621,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
                   v_ready = true;
                 }
                 const int n = pv_cnt[s];
-                if (ok) ok = wait_bar(bar(B_PFULLB + NPB * s + n % NPB), (n / NPB) & 1, ctl);
+                if (ok) ok = wait_bar(bar(B_PFULLB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
                 if (ok && j == 1) ok = wait_bar(bar(B_OEMPTY + s), (u_it & 1) ^ 1, ctl);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                pv_ss(s, n % NPB, j == 1, sdesc_lo(sKV + vslot * C::KVBYTES, 16));
+                pv_ss(s, n, j == 1, sdesc_lo(sKV + vslot * C::KVBYTES, 16));
                 ++pv_cnt[s];
                 if (j - 1 == U.n_s[s] - 1) ptx::tc_commit(bar(B_OFULL + s));
                 if (s == QST - 1) ptx::tc_commit(bar(B_KVEMPTY + vslot));
@@ -874,7 +857,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
     int p_cnt = 0;   // P tiles this warpgroup has handed to the MMA thread
     // shared-memory P: this thread's row of the tile's P buffer (K-major,
     // 128-byte swizzle: 8-row groups of 1024 bytes, 128 bytes per row)
-    const uint32_t prow0 = sP + NPB * s * C::PBYTES + (r >> 3) * 1024 + (r & 7) * 128;
+    const uint32_t prow0 = sP + 2 * s * C::PBYTES + (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = true;
     // a query tile that holds no rows in this launch (Nq <= 128) does nothing
     for (int it = 0; ok && s < n_active; ++it) {
@@ -996,11 +979,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         }
         const bool any_rescale = __any_sync(0xffffffffu, rescale);
         if constexpr (C::PSMEM) {
-          // P buffer p_cnt % NPBUF is free once PV number p_cnt - NPBUF is
-          // done; a rescale of O waits until after P is written (below)
-          if (p_cnt >= NPB) {
-            const int n = p_cnt - NPB;
-            ok = warp_wait_bar(bar(B_PFREEB + NPB * s + n % NPB), (n / NPB) & 1, ctl);
+          // P buffer p_cnt % 2 is free once PV number p_cnt - 2 is done; a
+          // rescale of O waits until after P is written (below)
+          if (p_cnt >= 2) {
+            const int n = p_cnt - 2;
+            ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
             if (!ok) break;
             ptx::tc_fence_after();
           }
@@ -1019,7 +1002,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         // chunks as they are produced (the whole S row is already in registers)
         const float nbias = bias_extra - mi;
         float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-        const uint32_t prow = prow0 + (uint32_t)(p_cnt % NPB) * C::PBYTES;   // shared-memory P
+        const uint32_t prow = prow0 + (uint32_t)(p_cnt & 1) * C::PBYTES;   // shared-memory P
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -1068,7 +1051,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
             // whole exponential phase to finish). The S registers are dead:
             // O is read 64 columns at a time with both loads in flight.
             const int n = p_cnt - 1;
-            ok = warp_wait_bar(bar(B_PFREEB + NPB * s + n % NPB), (n / NPB) & 1, ctl);
+            ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
             if (!ok) break;
             ptx::tc_fence_after();
             static_assert(D % 128 == 0, "O rescale in pairs of 64-column loads");
@@ -1099,8 +1082,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
         ptx::tc_fence_before();
         if constexpr (C::PSMEM) ptx::fence_proxy_async_smem();   // P visible to the MMA
         __syncwarp();
-        if (lane == 0)
-          ptx::mbar_arrive(bar(C::PSMEM ? B_PFULLB + NPB * s + p_cnt % NPB : B_PFULL + s));
+        if (lane == 0) ptx::mbar_arrive(bar(C::PSMEM ? B_PFULLB + 2 * s + (p_cnt & 1) : B_PFULL + s));
         ++p_cnt;
         if constexpr (DT == DT_E4M3) {
           if (j + 1 < ns) {
