@@ -242,19 +242,27 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
         }
       }
       if (signs) {
+        // the arithmetic is that of the scalar butterfly (each sum, difference
+        // and product rounded once), two values per packed FP32x2 instruction
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) y[i][v] *= sg[v];
+        for (int v = 0; v < VEC; v += 2)
+          ptx::mul2(y[i][v], y[i][v + 1], y[i][v], y[i][v + 1], sg[v], sg[v + 1]);
         // butterfly stages over the in-lane bits of the channel (the 3 bits
-        // within a chunk and the chunk-index bits above the lane bits)
+        // within a chunk and the chunk-index bits above the lane bits); from
+        // the second stage on, neighbouring values pair with neighbours
 #pragma unroll
-        for (int hs = 1; hs < VEC; hs <<= 1) {
+        for (int v = 0; v < VEC; v += 2) {
+          const float a = y[i][v], c = y[i][v + 1];
+          y[i][v] = a + c;
+          y[i][v + 1] = a - c;
+        }
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            if ((v & hs) == 0) {
-              const float a = y[i][v], c = y[i][v + hs];
-              y[i][v] = a + c;
-              y[i][v + hs] = a - c;
-            }
+        for (int hs = 2; hs < VEC; hs <<= 1) {
+#pragma unroll
+          for (int v = 0; v < VEC; v += 2) {
+            if ((v & hs) == 0)
+              ptx::addsub2(y[i][v], y[i][v + 1], y[i][v + hs], y[i][v + hs + 1], y[i][v],
+                           y[i][v + 1], y[i][v + hs], y[i][v + hs + 1]);
           }
         }
         // butterfly stages across the LPR lanes of the row: the lower lane
@@ -262,11 +270,12 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
 #pragma unroll
         for (int lm = 1; lm < LPR; lm <<= 1) {
           const float sgn = (hl & lm) ? -1.f : 1.f;
+          float other[VEC];
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            const float other = __shfl_xor_sync(0xffffffffu, y[i][v], lm);
-            y[i][v] = fmaf(y[i][v], sgn, other);
-          }
+          for (int v = 0; v < VEC; ++v) other[v] = __shfl_xor_sync(0xffffffffu, y[i][v], lm);
+#pragma unroll
+          for (int v = 0; v < VEC; v += 2)
+            ptx::fma2(y[i][v], y[i][v + 1], y[i][v], y[i][v + 1], sgn, sgn, other[v], other[v + 1]);
         }
         // the 1 / sqrt(d) of the transform is applied with the quantisation scale
       }

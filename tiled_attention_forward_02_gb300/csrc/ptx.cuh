@@ -362,6 +362,25 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1));
 }
+// (d0, d1) = (a0, a1) + (b0, b1), (e0, e1) = (a0, a1) - (b0, b1): two packed
+// FP32x2 instructions (round-to-nearest, as the scalar forms)
+__device__ __forceinline__ void addsub2(float& d0, float& d1, float& e0, float& e1, float a0,
+                                        float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd, re;\n\t"
+      "mov.b64 ra, {%4, %5};\n\tmov.b64 rb, {%6, %7};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tsub.rn.f32x2 re, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\tmov.b64 {%2, %3}, re;\n\t}"
+      : "=f"(d0), "=f"(d1), "=f"(e0), "=f"(e1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (d0, d1) = (a0, a1) * (b0, b1), one packed FP32x2 instruction
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 // pack two floats, round-to-nearest-even: `lo` in bits 0-15, `hi` in bits 16-31
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
