@@ -458,3 +458,46 @@ def test_prep_qkv_one_launch_equals_separate_calls(gpu_lib, variant, d):
             oc, ods, _ = ofp8.prepare(t.float().cpu().numpy(), None, False)
             np.testing.assert_array_equal(c.cpu().numpy(), oc)
             np.testing.assert_array_equal(ds.cpu().numpy(), ods)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_prep_qkv_claimed_tiles_bit_exact_repeated_and_on_two_streams(gpu_lib, d):
+    """A launch with several times more tiles than CTAs (most tiles are
+    claimed from the launch's counter while others run): codes and descales
+    are the oracle's, bit for bit (ragged last block, transposed V), on
+    every one of several calls in a row (each launch leaves its counter at
+    zero for the next), and two launches running at once on two streams give
+    the codes of sequential calls."""
+    B, N, H = 2, 4000, 16
+    q, k, v = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=26,
+                                outlier_frac=1e-3, device="cuda")
+    first = gpu_lib.attn_prep_fp8_qkv(q, k, v)
+    assert gpu_lib.get_status() == 0
+    for t, c, ds in ((q, first[0], first[1]), (k, first[2], first[3])):
+        oc, ods, _ = ofp8.prepare(t.float().cpu().numpy(), None, False)
+        np.testing.assert_array_equal(ds.cpu().numpy(), ods)
+        np.testing.assert_array_equal(c.cpu().numpy(), oc)
+    oc, ods, _ = ofp8.prepare(v.float().cpu().numpy(), None, False)
+    np.testing.assert_array_equal(first[5].cpu().numpy(), ods)
+    np.testing.assert_array_equal(first[4].cpu().numpy()[..., :N], oc.transpose(0, 2, 3, 1))
+    for _ in range(5):
+        again = gpu_lib.attn_prep_fp8_qkv(q, k, v)
+        for g, w in zip(again, first):
+            assert torch.equal(g, w)
+    # a second problem, prepared alone, then both at once on two streams
+    q2, k2, v2 = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=27,
+                                   outlier_frac=1e-3, device="cuda")
+    alone = gpu_lib.attn_prep_fp8_qkv(q2, k2, v2)
+    out1 = tuple(torch.empty_like(t) for t in first)
+    out2 = tuple(torch.empty_like(t) for t in alone)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        gpu_lib.attn_prep_fp8_qkv(q, k, v, out=out1, stream=s1)
+        gpu_lib.attn_prep_fp8_qkv(q2, k2, v2, out=out2, stream=s2)
+    torch.cuda.synchronize()
+    assert gpu_lib.get_status() == 0
+    for g, w in zip(out1, first):
+        assert torch.equal(g, w)
+    for g, w in zip(out2, alone):
+        assert torch.equal(g, w)

@@ -26,12 +26,25 @@ struct DeviceState {
   int cc_major = 0, cc_minor = 0;
   int smem_optin = 0;
   unsigned int* status = nullptr;  // device status word (timeouts, internal checks)
+  // tile counters of the prep launches: kPrepSlots pairs (next tile,
+  // finished CTAs), each left at zero by the launch that used it
+  unsigned long long* prep_sched = nullptr;
 };
+constexpr int kPrepSlots = 64;
+constexpr size_t kStatusBlockBytes = 256 + kPrepSlots * 2 * sizeof(unsigned long long);
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_launches{0};
+std::atomic<unsigned> g_prep_seq{0};
+
+// the tile counter of one prep call: slots are taken in turn, so that up to
+// kPrepSlots prep launches may run at the same time (on different streams)
+// without sharing a counter
+unsigned long long* prep_slot(const DeviceState* st) {
+  return st->prep_sched + 2 * (g_prep_seq.fetch_add(1) % kPrepSlots);
+}
 thread_local char g_cuda_msg[256] = "no CUDA error recorded";
 
 // one-time per-device set-up; returns 0 or an error code
@@ -48,10 +61,14 @@ int device_state(DeviceState** out) {
     if ((rc = device_attrs(dev, &st.sm_count, &st.cc_major, &st.cc_minor)) != ATTN_OK) return rc;
     if ((e = cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)))
       return cuda_fail(e, "cudaDeviceGetAttribute");
-    if ((e = cudaMalloc(&st.status, sizeof(unsigned int))) != cudaSuccess)
+    // one allocation: the status word, then the prep launches' tile counters
+    void* blk = nullptr;
+    if ((e = cudaMalloc(&blk, kStatusBlockBytes)) != cudaSuccess)
       return cuda_fail(e, "cudaMalloc(status word)");
-    if ((e = cudaMemset(st.status, 0, sizeof(unsigned int))) != cudaSuccess)
+    if ((e = cudaMemset(blk, 0, kStatusBlockBytes)) != cudaSuccess)
       return cuda_fail(e, "cudaMemset(status word)");
+    st.status = static_cast<unsigned int*>(blk);
+    st.prep_sched = reinterpret_cast<unsigned long long*>(static_cast<char*>(blk) + 256);
     st.ready = true;
   }
   // the kernels are built for sm_103a only
@@ -300,7 +317,8 @@ extern "C" int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int
   if ((rc = map_prep(&mx, x, B, N, H, d)) != ATTN_OK) return rc;
   const int group = signs ? H / sign_heads : 1;
   return launch_prep_fp8(mx, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
-                         nullptr, 0, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
+                         nullptr, 0, st->sm_count, st->status, prep_slot(st),
+                         static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_prep_fp8_per_tensor(const void* x, void* x8, float* descale, int B, int H,
@@ -314,7 +332,8 @@ extern "C" int attn_prep_fp8_per_tensor(const void* x, void* x8, float* descale,
   if ((rc = map_prep(&mx, x, B, N, H, d)) != ATTN_OK) return rc;
   const int group = signs ? H / sign_heads : 1;
   return launch_prep_fp8(mx, x8, descale, B, H, (int)N, d, signs, group, transpose_out, nullptr,
-                         nullptr, 1, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
+                         nullptr, 1, st->sm_count, st->status, prep_slot(st),
+                         static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int attn_prep_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8,
@@ -356,6 +375,7 @@ extern "C" int attn_prep_fp8_qkv(const void* q, const void* k, const void* v, vo
   J.n_jobs = n;
   J.any_transpose = Nk > 0 ? 1 : 0;
   J.n_tiles = tiles;
+  J.sched = prep_slot(st);
   return launch_prep_jobs(J, d, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
 }
 
@@ -387,7 +407,7 @@ extern "C" int attn_prep_fp8_rope(const void* x, void* x8, float* descale, int B
   if ((rc = map_prep(&mx, x, B, N, H, d)) != ATTN_OK) return rc;
   const int group = signs ? H / sign_heads : 1;
   return launch_prep_fp8(mx, x8, descale, B, H, (int)N, d, signs, group, 0, rope_cos, rope_sin, 0,
-                         st->sm_count, st->status, static_cast<cudaStream_t>(stream));
+                         st->sm_count, st->status, prep_slot(st), static_cast<cudaStream_t>(stream));
 }
 
 namespace attn {

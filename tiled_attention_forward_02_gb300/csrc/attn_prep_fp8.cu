@@ -8,14 +8,16 @@
 // Hadamard x random signs, to spread outliers before quantisation).
 //
 // A tile is one (128-token block, head, batch).  Persistent CTAs (two per SM
-// for d <= 128) walk the tiles with heads varying fastest; each CTA keeps a
-// ring of NS tiles in shared memory filled by TMA copies (one 128 x d box per
-// tile, rows past N zero-filled), so the next tiles stream in while the
-// current one is transformed and quantised.  8 warps x 16 rows; LPR lanes
-// hold one row (8 for d <= 128, 16 for d = 256), lane l owning the 16-byte
-// chunks l, l + LPR, ... of 8 channels each, so that 8 lanes read 128
-// contiguous bytes of shared memory (no bank conflicts) and the rotary pair
-// (c, c + d/2) lies in one lane for d >= 128.  The transform is a fast
+// for d <= 128) walk the tiles with heads varying fastest, taking tiles from
+// a per-launch counter after their first few; each CTA keeps a ring of NS
+// tiles in shared memory filled by TMA copies (one 128 x d box per tile, rows
+// past N zero-filled), so the next tiles stream in while the current one is
+// transformed and quantised.  8 warps x 16 rows; LPR lanes hold one row (8
+// for d <= 128, 16 for d = 256), lane l owning the 16-byte chunks l, l + LPR,
+// ... of 8 channels each, so that 8 lanes read 128 contiguous bytes of shared
+// memory (no bank conflicts) and the rotary pair (c, c + d/2) lies in one
+// lane for d >= 128; a thread holds 16 LPR / 32 consecutive rows, so that
+// four of them give one 4-byte word per channel of the transposed layout.  The transform is a fast
 // Walsh-Hadamard butterfly (stages over the in-lane channel bits, then
 // shuffles across the LPR lanes of the row), scaled by 1/sqrt(d); the
 // block amax is reduced through shared memory; descale = amax / 448 (float32);
@@ -69,7 +71,7 @@ struct PrepCfg {
   static constexpr int CH = D / (8 * LPR);          // 16-byte chunks (8 channels) per lane
   static constexpr int NS = D == 64 ? 4 : 3;        // tiles in flight per CTA
   static constexpr int CTAS_PER_SM = D == 256 ? 1 : 2;
-  static constexpr int TAIL = 256;                  // barriers, amax scratch, flags
+  static constexpr int TAIL = 256;                  // barriers, amax slots, stage tiles
   static int smem_bytes(int transpose_out) {
     return 128 + NS * TILE_BYTES + (transpose_out ? D * 128 : 0) + TAIL;
   }
@@ -85,9 +87,27 @@ enum PrepMode : int {
   kPrepTensor = 2,      // per-tensor, second pass: codes from the tensor amax
 };
 
+// Word index, within a 128-key row e of the transposed staging tile, where
+// logical word kw (keys 4 kw .. 4 kw + 3) is kept: XOR-swizzled by the
+// channel's 8-channel chunk so that the 32 lanes of one staging store (32
+// different rows e, lanes holding 4 consecutive keys each) hit 32 banks.
+template <int LPR>
+__device__ __forceinline__ int tr_word(int e, int kw) {
+  if constexpr (LPR == 8) {
+    return kw ^ (((e >> 3) & 7) << 2);
+  } else {
+    const int h = (e >> 3) & 15;
+    return kw ^ ((h & 1) | ((h >> 1) << 2));
+  }
+}
+
 // A launch walks the tiles of up to three tensors (Q, K, V of one attention
 // call) one tensor after the other, so that the ramp-up and the tail of a
 // persistent launch (about 7 us) are paid once per step instead of per tensor.
+// Each CTA's first NS tiles are fixed (tile blockIdx + s * grid); every later
+// tile is claimed from a counter (J.sched[0]), so that CTAs on faster SMs take
+// more tiles and all of them end within about one tile of each other. The
+// last CTA to finish sets the counter back to zero for the next launch.
 template <int D, int MODE, bool ROPE>
 __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     prep_fp8_kernel(const __grid_constant__ PrepJobs J, float* tensor_amax, unsigned int* status) {
@@ -95,9 +115,10 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   constexpr int LPR = PC::LPR;        // lanes per row
   constexpr int CH = PC::CH;          // chunks of 8 channels per lane
   constexpr int VEC = 8 * CH;         // channels per lane
-  constexpr int RPW = 32 / LPR;       // rows per warp and iteration
-  constexpr int ITERS = 16 / RPW;     // 8 warps x 16 rows = 128 rows
+  constexpr int RPW = 32 / LPR;       // row groups per warp
+  constexpr int ITERS = 16 / RPW;     // consecutive rows per thread (8 warps x 16 rows)
   constexpr int NS = PC::NS;
+  static_assert(ITERS % 4 == 0, "rows are staged for the transpose four at a time");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = ptx::smem_addr(smem_raw);
   const uint32_t pad = (128u - (sraw & 127u)) & 127u;
@@ -105,14 +126,18 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   const uint32_t sbase = sraw + pad;                           // NS tiles
   uint8_t* s_t = smem + NS * PC::TILE_BYTES;                   // transposed codes
   uint8_t* tail = s_t + (J.any_transpose ? D * 128 : 0);
+  static_assert(NS <= 4, "tail layout");
   uint64_t* bars = reinterpret_cast<uint64_t*>(tail);          // [NS] tile landed
-  float* s_amax = reinterpret_cast<float*>(tail + 8 * NS);     // [2][8]
+  float* s_amax = reinterpret_cast<float*>(tail + 32);         // [2][8], 16-byte aligned
+  long long* s_tile = reinterpret_cast<long long*>(tail + 96); // [NS] tile of a stage
   auto bar = [&](int i) { return ptx::smem_addr(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rsub = lane / LPR, hl = lane % LPR;
   // channel of value v = 8 j + t of this lane: 8 (hl + LPR j) + t
   auto chan = [&](int v) { return 8 * (hl + LPR * (v >> 3)) + (v & 7); };
+  // row of the tile held in iteration i: rows r0 .. r0 + ITERS - 1
+  const int r0 = warp * 16 + ITERS * rsub;
   const long long n_tiles = J.n_tiles;
   const long long G = gridDim.x;
   // tensor of tile t, its parameters and its tensor map (constant indices
@@ -130,26 +155,57 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     for (int jj = 0; jj < J.n_jobs; ++jj) ptx::tma_prefetch_desc(map_of(jj));
   }
   __syncthreads();
-  // tile t of a tensor: heads fastest, then blocks, then batch
-  auto issue = [&](long long k) {   // copy the CTA's k-th tile into stage k % NS
-    const long long t = blockIdx.x + k * G;
-    if (t >= n_tiles) return;
+  // (thread 0) stage st receives tile t, or the end mark when t is past the
+  // last tile; the tile index is written before the arrival that completes
+  // the stage's phase, so a thread that saw the phase complete reads it
+  auto issue = [&](int st, long long t) {
+    if (t >= n_tiles) {
+      s_tile[st] = -1;
+      ptx::mbar_arrive(bar(st));
+      return;
+    }
+    s_tile[st] = t;
     const int jj = job_of(t);
     const PrepJob jb = job(jj);
     const long long tl = t - jb.tile0;
     const int th = (int)(tl % jb.H);
     const long long r = tl / jb.H;
     const int tblk = (int)(r % jb.nb), tb = (int)(r / jb.nb);
-    const int st = (int)(k % NS);
     ptx::mbar_arrive_expect_tx(bar(st), PC::TILE_BYTES);
     ptx::tma_load_4d(sbase + st * PC::TILE_BYTES, map_of(jj), bar(st), 0, th, tblk * 128, tb);
   };
-  if (threadIdx.x == 0)
-    for (int k = 0; k < NS; ++k) issue(k);
+  // (thread 0) the tile for the next refill, claimed one tile ahead of its
+  // use so that the counter's round trip stays off the refill path
+  long long claim = n_tiles;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < NS; ++k) issue(k, blockIdx.x + k * G);
+    if (blockIdx.x + (NS - 1) * G < n_tiles)
+      claim = NS * G + (long long)atomicAdd(J.sched, 1ull);
+  }
+  // (thread 0) once this CTA is done: count it, and let the last CTA of the
+  // launch reset the counter (every claim of every CTA precedes its count)
+  auto finish = [&]() {
+    __threadfence();
+    if (atomicAdd(J.sched + 1, 1ull) == (unsigned long long)(G - 1)) {
+      J.sched[0] = 0;
+      J.sched[1] = 0;
+      __threadfence();
+    }
+  };
 
   for (long long k = 0;; ++k) {
-    const long long t = blockIdx.x + k * G;
-    if (t >= n_tiles) break;
+    const int st = (int)(k % NS);
+    // bounded wait for the stage; every thread takes the same decision: a
+    // stage holding the end mark completed its phase before any thread got
+    // here, and one holding a tile goes to the amax barrier below
+    bool ok = ptx::mbar_try_wait(bar(st), (uint32_t)((k / NS) & 1));
+    if (!ok) {
+      const long long t0 = clock64();
+      while (!(ok = ptx::mbar_try_wait_sleep(bar(st), (uint32_t)((k / NS) & 1), 100000)))
+        if (clock64() - t0 > kPrepWaitCycles) break;
+    }
+    const long long t = ok ? s_tile[st] : 0;
+    if (t < 0) break;
     const PrepJob jb = job(job_of(t));
     const int H = jb.H, N = jb.N, nb = jb.nb, Npad = jb.Npad;
     const int transpose_out = jb.transpose_out, sign_group = jb.sign_group;
@@ -162,42 +218,32 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     const int h = (int)(tl % H);
     const long long rr = tl / H;
     const int blk = (int)(rr % nb), b = (int)(rr / nb);
-    const int st = (int)(k % NS);
-    // bounded wait for the tile; every thread takes the same decision
-    bool ok = ptx::mbar_try_wait(bar(st), (uint32_t)((k / NS) & 1));
-    if (!ok) {
-      const long long t0 = clock64();
-      while (!(ok = ptx::mbar_try_wait_sleep(bar(st), (uint32_t)((k / NS) & 1), 100000)))
-        if (clock64() - t0 > kPrepWaitCycles) break;
-    }
     // (a thread whose wait gave up reads stale data; the block leaves at the
     // amax barrier below, before anything is stored)
-    // row of iteration i within the tile: warp*16 + RPW*i + rsub
-    auto row_of = [&](int i) { return blk * 128 + warp * 16 + RPW * i + rsub; };
+    const int n0 = blk * 128 + r0;   // token of iteration 0
     const uint32_t tile = sbase + st * PC::TILE_BYTES;
 
-    // signs of this lane's channels: chunk j is 8 consecutive channels, one
-    // 8-byte load (the host requires 8-byte aligned signs)
-    float sg[VEC];
-#pragma unroll
-    for (int j = 0; j < CH; ++j) {
-      uint2 w = make_uint2(0x01010101u, 0x01010101u);
-      if (signs)
-        w = __ldg(reinterpret_cast<const uint2*>(signs + (long long)(h / sign_group) * D +
-                                                 8 * (hl + LPR * j)));
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        sg[8 * j + t] = (float)(int8_t)(((t < 4 ? w.x : w.y) >> (8 * (t & 3))) & 0xFFu);
-    }
-
     float y[ITERS][VEC];
-    // the whole tile from shared memory (rows past N were zero-filled by the copy)
+    // the thread's rows from shared memory (rows past N were zero-filled by the copy)
 #pragma unroll
     for (int i = 0; i < ITERS; ++i)
 #pragma unroll
       for (int j = 0; j < CH; ++j)
-        load_chunk(tile + (uint32_t)((warp * 16 + RPW * i + rsub) * D * 2 + (hl + LPR * j) * 16),
-                   &y[i][8 * j]);
+        load_chunk(tile + (uint32_t)((r0 + i) * D * 2 + (hl + LPR * j) * 16), &y[i][8 * j]);
+
+    // signs of this lane's channels: chunk j is 8 consecutive channels, one
+    // 8-byte load (the host requires 8-byte aligned signs)
+    float sg[VEC];
+    if (signs) {
+#pragma unroll
+      for (int j = 0; j < CH; ++j) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(
+            signs + (long long)(h / sign_group) * D + 8 * (hl + LPR * j)));
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          sg[8 * j + q] = (float)(int8_t)(((q < 4 ? w.x : w.y) >> (8 * (q & 3))) & 0xFFu);
+      }
+    }
 
     float amax = 0.f;
 #pragma unroll
@@ -206,11 +252,14 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
         // (y_c, y_{c+D/2}) -> (y_c cos - y_{c+D/2} sin, y_{c+D/2} cos + y_c sin).
         // With two or more chunks per lane the partner of chunk j is chunk
         // j ^ CH/2 of the same lane; with one (d = 64) it is lane hl ^ LPR/2.
-        const int n = row_of(i);
-        float cs[VEC], sn[VEC];
+        const int n = n0 + i;
+        // channels c and c + D/2 share angle c: with two or more chunks per
+        // lane the upper half of the lane's values reuses the lower half's
+        constexpr int HV = CH >= 2 ? VEC / 2 : VEC;
+        float cs[HV], sn[HV];
         if (n < N) {
 #pragma unroll
-          for (int v = 0; v < VEC; v += 4) {
+          for (int v = 0; v < HV; v += 4) {
             const int c = chan(v) % (D / 2);
             const float4 c4 = __ldg(reinterpret_cast<const float4*>(rope_cos + (long long)n * (D / 2) + c));
             const float4 s4 = __ldg(reinterpret_cast<const float4*>(rope_sin + (long long)n * (D / 2) + c));
@@ -219,25 +268,23 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
           }
         } else {
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) { cs[v] = 1.f; sn[v] = 0.f; }
+          for (int v = 0; v < HV; ++v) { cs[v] = 1.f; sn[v] = 0.f; }
         }
         if constexpr (CH >= 2) {
-          float r[VEC];
+          // value v < HV (chunk j < CH/2) pairs with v + HV (chunk j + CH/2)
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            const int pv = v ^ (4 * CH);   // chunk j ^ CH/2, same offset in the chunk
-            const bool upper = (v & (4 * CH)) != 0;
-            r[v] = fmaf(y[i][v], cs[v], upper ? y[i][pv] * sn[v] : -(y[i][pv] * sn[v]));
+          for (int v = 0; v < HV; ++v) {
+            const float lo = y[i][v], hi = y[i][v + HV];
+            y[i][v] = fmaf(lo, cs[v], -(hi * sn[v]));
+            y[i][v + HV] = fmaf(hi, cs[v], lo * sn[v]);
           }
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) y[i][v] = r[v];
         } else {
           const bool upper = (hl & (LPR / 2)) != 0;
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
             const float other = __shfl_xor_sync(0xffffffffu, y[i][v], LPR / 2);
-            const float t = upper ? other * sn[v] : -(other * sn[v]);
-            y[i][v] = fmaf(y[i][v], cs[v], t);
+            const float tt = upper ? other * sn[v] : -(other * sn[v]);
+            y[i][v] = fmaf(y[i][v], cs[v], tt);
           }
         }
       }
@@ -280,7 +327,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
         // the 1 / sqrt(d) of the transform is applied with the quantisation scale
       }
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) amax = fmaxf(amax, fabsf(y[i][v]));
+      for (int v = 0; v < VEC; v += 2) amax = ptx::max3(amax, fabsf(y[i][v]), fabsf(y[i][v + 1]));
     }
 
     float bmax;
@@ -303,21 +350,28 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
         atomicOr(status, 1u);
         // wait (bounded) for the copies this CTA still has in flight
         for (long long kk = k; kk < k + NS; ++kk) {
-          if (blockIdx.x + kk * G >= n_tiles) break;
+          const int sk = (int)(kk % NS);
+          if (s_tile[sk] < 0) break;
           const long long t0 = clock64();
-          while (!ptx::mbar_try_wait(bar((int)(kk % NS)), (uint32_t)((kk / NS) & 1)))
+          while (!ptx::mbar_try_wait(bar(sk), (uint32_t)((kk / NS) & 1)))
             if (clock64() - t0 > kPrepWaitCycles) break;
         }
+        finish();
       }
       return;
     }
-    if (threadIdx.x == 0) issue(k + NS);   // stage st is free: the tile NS ahead
+    if (threadIdx.x == 0) {
+      // stage st is free: the claimed tile goes there, the next one is claimed
+      issue(st, claim);
+      if (claim < n_tiles) claim = NS * G + (long long)atomicAdd(J.sched, 1ull);
+    }
     if constexpr (MODE == kPrepTensor) {
       bmax = *tensor_amax;   // written by the amax pass, read-only here
     } else {
-      bmax = amax_slot[0];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) bmax = fmaxf(bmax, amax_slot[w]);
+      const float4 a0 = *reinterpret_cast<const float4*>(amax_slot);
+      const float4 a1 = *reinterpret_cast<const float4*>(amax_slot + 4);
+      bmax = fmaxf(ptx::max3(a0.x, a0.y, a0.z), ptx::max3(a0.w, a1.x, a1.y));
+      bmax = ptx::max3(bmax, a1.z, a1.w);
       if (signs) bmax *= inv_sqrt_d;
     }
     if constexpr (MODE == kPrepTensorAmax) {
@@ -356,43 +410,64 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
       if (threadIdx.x == 0) descale[((long long)b * H + h) * nb + blk] = ds;
     }
 
+    // codes, four rows at a time: word q of row i holds channels 4q .. 4q + 3
+    // of the lane
 #pragma unroll
-    for (int i = 0; i < ITERS; ++i) {
-      const int n = row_of(i);
-      const int nl = n - blk * 128;
-      uint32_t c4[VEC / 4];
-      if (!divide) {
+    for (int g = 0; g < ITERS / 4; ++g) {
+      uint32_t c4[4][VEC / 4];
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q)
-          c4[q] = ptx::pack_e4m3x4(y[i][4 * q] * inv_ds, y[i][4 * q + 1] * inv_ds,
-                                   y[i][4 * q + 2] * inv_ds, y[i][4 * q + 3] * inv_ds);
-      } else {
-        auto quot = [&](float x) {
-          const float q0 = x * inv_ds;
-          const float res = fmaf(-q0, ds, x);
-          return res == 0.f ? q0 : fmaf(res, inv_ds, q0);   // (keeps the sign of a zero)
-        };
+      for (int ii = 0; ii < 4; ++ii) {
+        const int i = 4 * g + ii;
+        if (!divide) {
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q)
-          c4[q] = ptx::pack_e4m3x4(quot(y[i][4 * q]), quot(y[i][4 * q + 1]),
-                                   quot(y[i][4 * q + 2]), quot(y[i][4 * q + 3]));
-      }
-      if (!transpose_out) {
-        if (n < N) {
-          // chunk j of the lane: 8 codes at channel 8 (hl + LPR j)
-          uint8_t* dst = x8 + (((long long)b * N + n) * H + h) * D;
+          for (int q = 0; q < VEC / 4; ++q) {
+            float p0, p1, p2, p3;
+            ptx::mul2(p0, p1, y[i][4 * q], y[i][4 * q + 1], inv_ds, inv_ds);
+            ptx::mul2(p2, p3, y[i][4 * q + 2], y[i][4 * q + 3], inv_ds, inv_ds);
+            c4[ii][q] = ptx::pack_e4m3x4(p0, p1, p2, p3);
+          }
+        } else {
+          auto quot = [&](float x) {
+            const float q0 = x * inv_ds;
+            const float res = fmaf(-q0, ds, x);
+            return res == 0.f ? q0 : fmaf(res, inv_ds, q0);   // (keeps the sign of a zero)
+          };
 #pragma unroll
-          for (int j = 0; j < CH; ++j)
-            *reinterpret_cast<uint2*>(dst + 8 * (hl + LPR * j)) = make_uint2(c4[2 * j], c4[2 * j + 1]);
+          for (int q = 0; q < VEC / 4; ++q)
+            c4[ii][q] = ptx::pack_e4m3x4(quot(y[i][4 * q]), quot(y[i][4 * q + 1]),
+                                         quot(y[i][4 * q + 2]), quot(y[i][4 * q + 3]));
         }
-      } else {
-        // stage codes channel-major: s_t[e][nl ^ swz(e)] (rows n >= N hold
-        // zeros); swz(e) = (chunk of e) x 4 puts the chunks written by one
-        // store in distinct banks (rows of a warp share a 4-byte word)
+        if (!transpose_out) {
+          const int n = n0 + i;
+          if (n < N) {
+            // chunk j of the lane: 8 codes at channel 8 (hl + LPR j)
+            uint8_t* dst = x8 + (((long long)b * N + n) * H + h) * D;
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-          const int e = chan(v);
-          s_t[e * 128 + (nl ^ (((e >> 3) & 31) << 2))] = (uint8_t)((c4[v >> 2] >> (8 * (v & 3))) & 0xFF);
+            for (int j = 0; j < CH; ++j)
+              *reinterpret_cast<uint2*>(dst + 8 * (hl + LPR * j)) =
+                  make_uint2(c4[ii][2 * j], c4[ii][2 * j + 1]);
+          }
+        }
+      }
+      if (transpose_out) {
+        // stage codes channel-major: row e of s_t holds the 128 keys of
+        // channel e. The lane's rows are consecutive keys, so four rows give
+        // one 4-byte word per channel: a 4 x 4 byte transpose of the words of
+        // four rows (rows n >= N hold zeros)
+        const int kw = (r0 + 4 * g) >> 2;
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+          const uint32_t lo01 = __byte_perm(c4[0][q], c4[1][q], 0x5140);
+          const uint32_t hi01 = __byte_perm(c4[0][q], c4[1][q], 0x7362);
+          const uint32_t lo23 = __byte_perm(c4[2][q], c4[3][q], 0x5140);
+          const uint32_t hi23 = __byte_perm(c4[2][q], c4[3][q], 0x7362);
+          const uint32_t w[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                                 __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int e = chan(4 * q + c);
+            reinterpret_cast<uint32_t*>(s_t)[e * 32 + tr_word<LPR>(e, kw)] = w[c];
+          }
         }
       }
     }
@@ -404,11 +479,12 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
         if (lane * 4 < valid) {
           uint8_t* dst = x8 + (((long long)b * H + h) * D + e) * Npad + blk * 128 + lane * 4;
           *reinterpret_cast<uint32_t*>(dst) =
-              *reinterpret_cast<const uint32_t*>(&s_t[e * 128 + ((lane * 4) ^ (((e >> 3) & 31) << 2))]);
+              reinterpret_cast<const uint32_t*>(s_t)[e * 32 + tr_word<LPR>(e, lane)];
         }
       }
     }
   }
+  if (threadIdx.x == 0) finish();
 }
 
 // descale of every block from the tensor amax in descale[0]; one CTA, every
@@ -497,8 +573,9 @@ int launch_prep_jobs(const PrepJobs& J, int d, int sm_count, unsigned int* statu
 int launch_prep_fp8(const CUtensorMap& map_x, void* x8, float* descale, int B, int H, int N, int d,
                     const int8_t* signs, int sign_group, int transpose_out, const float* rope_cos,
                     const float* rope_sin, int per_tensor, int sm_count, unsigned int* status,
-                    cudaStream_t stream) {
+                    unsigned long long* sched, cudaStream_t stream) {
   PrepJobs J{};
+  J.sched = sched;
   J.map[0] = map_x;
   J.job[0] = prep_job(x8, descale, B, H, N, signs, sign_group, transpose_out, rope_cos, rope_sin, 0);
   J.n_jobs = 1;

@@ -83,13 +83,16 @@ struct PrepJob {
   int sign_group, H, N, nb, Npad, transpose_out;
 };
 // up to three tensors in one launch; map[i]: tensor i's bf16 input as
-// (d, H, N, B), box d x 1 x 128 x 1, no swizzle
+// (d, H, N, B), box d x 1 x 128 x 1, no swizzle; sched: the launch's tile
+// counter and finished-CTA count, both zero before the launch (the kernel
+// leaves them zero)
 struct PrepJobs {
   CUtensorMap map[3];
   PrepJob job[3];
   int n_jobs;
   int any_transpose;
   long long n_tiles;
+  unsigned long long* sched;
 };
 PrepJob prep_job(void* x8, float* descale, int B, int H, int N, const int8_t* signs,
                  int sign_group, int transpose_out, const float* rope_cos, const float* rope_sin,
@@ -105,7 +108,7 @@ int launch_prep_jobs(const PrepJobs& J, int d, int sm_count, unsigned int* statu
 int launch_prep_fp8(const CUtensorMap& map_x, void* x8, float* descale, int B, int H, int N, int d,
                     const int8_t* signs, int sign_group, int transpose_out, const float* rope_cos,
                     const float* rope_sin, int per_tensor, int sm_count, unsigned int* status,
-                    cudaStream_t stream);
+                    unsigned long long* sched, cudaStream_t stream);
 int launch_rope_table(float* cos_out, float* sin_out, int N, int d, double base, long long pos0,
                       cudaStream_t stream);
 
