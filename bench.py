@@ -42,6 +42,7 @@ WORKLOADS = {
     "bf16_causal_gqa_B1_Hq64_Hkv8_N131072_d128": (1, 64, 8, 131072, 131072, 128, True, "bf16"),
     "fp8_e4m3_B4_H16_N4096_d128": (4, 16, 16, 4096, 4096, 128, False, "fp8"),
     "fp8_e4m3_hadamard_B4_H16_N4096_d128": (4, 16, 16, 4096, 4096, 128, False, "fp8h"),
+    "fp8_e4m3_B4_H16_N4096_d64": (4, 16, 16, 4096, 4096, 64, False, "fp8"),
     "fp8_e4m3_B4_H16_N4096_d256": (4, 16, 16, 4096, 4096, 256, False, "fp8"),
     "fp8_e4m3_causal_gqa_B1_Hq64_Hkv8_N32768_d128": (1, 64, 8, 32768, 32768, 128, True, "fp8"),
     # rotary embedding fused into the Q / K prep (tables built once, outside the steps)

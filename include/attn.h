@@ -228,7 +228,7 @@ int attn_prep_fp8_qkv(const void* q, const void* k, const void* v, void* q8, voi
  *             zero (attn_prep_fp8 with transpose_out = 1)
  *                                                 v_descale [B, Hkv, ceil(Nk/128)]
  *   o         [B, Nq, Hq, d] bfloat16 (written)   lse [B, Hq, Nq] float32 (written)
- *   d         128 or 256
+ *   d         64, 128 or 256
  *   hadamard  0 or 1: states whether Q and K went through the transform; the
  *             arithmetic does not change (Q M (K M)^T = Q K^T), the flag is
  *             validated and kept for the caller's bookkeeping.

@@ -83,9 +83,9 @@ def test_fp8_and_prep_reject_bad_arguments_on_host(lib):
     assert L.attn_prep_fp8(A, A, A, 1, 4, 100, 128, A, 3, 0, None) == attn.ERR_INVALID_ARG
     assert L.attn_prep_fp8(A + 8, A, A, 1, 4, 100, 128, None, 0, 0, None) == attn.ERR_MISALIGNED
     assert L.attn_prep_fp8(A, A, A, 0, 4, 100, 128, None, 0, 0, None) == attn.OK
-    # fp8 forward: d = 64 not covered, bad hadamard flag, null descale
+    # fp8 forward: d = 96 not covered, bad hadamard flag, null descale
     args = [A, A, A, A, A, A, A, A, 1, 2, 2, 10, 10, 128, 0, 0.1, 0, None]
-    bad = list(args); bad[13] = 64
+    bad = list(args); bad[13] = 96
     assert L.attn_fwd_fp8(*bad) == attn.ERR_UNSUPPORTED
     bad = list(args); bad[16] = 2
     assert L.attn_fwd_fp8(*bad) == attn.ERR_INVALID_ARG

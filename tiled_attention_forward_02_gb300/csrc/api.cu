@@ -116,15 +116,17 @@ int encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const cuu
 }
 
 // BSHD tensor [B, N, H, d] as TMA dims (d, H, N, B); box = `heads` heads x
-// 128 / heads rows (128 rows of 128 bytes in all), `inner` elements of d
-// (128 bytes for the 128-byte swizzle)
+// 128 / heads rows (128 rows in all), `inner` elements of d: 128 bytes for
+// the 128-byte swizzle, or 64 bytes (a whole FP8 row of d = 64) for the
+// 64-byte swizzle
 int map_bshd(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* base, int B, int64_t N,
              int H, int d, int inner, int heads) {
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)d * esz, (cuuint64_t)H * d * esz,
                                  (cuuint64_t)N * H * d * esz};
   const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)heads, (cuuint32_t)(128 / heads), 1};
-  return encode(map, dt, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode(map, dt, base, dims, strides, box,
+                inner * esz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 namespace {
@@ -258,7 +260,7 @@ extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
   int rc = check_common(B, Hq, Hkv, Nq, Nk, causal, scale);
   if (rc < 0) return rc;
   if (hadamard != 0 && hadamard != 1) return ATTN_ERR_INVALID_ARG;
-  if (d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (rc == 1) return ATTN_OK;
   if (!q8 || !k8 || !v8t || !q_descale || !k_descale || !v_descale || !o || !lse)
     return ATTN_ERR_INVALID_ARG;
@@ -270,9 +272,10 @@ extern "C" int attn_fwd_fp8(const void* q8, const void* k8, const void* v8t,
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != ATTN_OK) return rc;
   const int64_t Npad = (Nk + 15) / 16 * 16;
+  const int inner = d == 64 ? 64 : 128;   // bytes of a row chunk (64-byte rows at d = 64)
   CUtensorMap mq, mk, mv;
-  if ((rc = map_bshd(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q8, B, Nq, Hq, d, 128, 1)) ||
-      (rc = map_bshd(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k8, B, Nk, Hkv, d, 128, 1)) ||
+  if ((rc = map_bshd(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q8, B, Nq, Hq, d, inner, 1)) ||
+      (rc = map_bshd(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, k8, B, Nk, Hkv, d, inner, 1)) ||
       (rc = map_vt(&mv, v8t, B, Hkv, d, Npad)))
     return rc;
   FwdParams p{};

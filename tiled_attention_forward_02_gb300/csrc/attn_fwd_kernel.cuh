@@ -93,9 +93,12 @@ struct FwdCfg {
   static constexpr int BN = 128;
   static constexpr int QST = (D == 256) ? 1 : 2;   // query tiles per unit (TMEM budget)
   static constexpr int ROWB = D * ELT;              // bytes of one Q/K row
-  static constexpr int NCH = ROWB / 128;            // 128-byte swizzle chunks per row
-  static constexpr int CH_ELEMS = 128 / ELT;        // elements per chunk
-  static constexpr int CHUNK_BYTES = 128 * 128;     // one chunk of 128 rows
+  // Q and K tiles: 128-byte swizzle in chunks of 128 bytes per row; a 64-byte
+  // row (FP8, d = 64) is one chunk with the 64-byte swizzle
+  static constexpr int SWZ = ROWB >= 128 ? 128 : 64;
+  static constexpr int NCH = ROWB / SWZ;            // swizzle chunks per row
+  static constexpr int CH_ELEMS = SWZ / ELT;        // elements per chunk
+  static constexpr int CHUNK_BYTES = 128 * SWZ;     // one chunk of 128 rows
   static constexpr int QBYTES = BM * ROWB;
   static constexpr int KVBYTES = BN * ROWB;         // K tile; V (or V^T) tile is the same size
   static constexpr int SMEM_LIMIT = 232448;         // 227 KB opt-in per CTA
@@ -152,18 +155,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 // memory offsets stay below 2^18 bytes, so adding (offset >> 4) to the low
 // word never carries out of the field: one add per MMA operand.
 constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
+// the same for 64-byte rows: 64-byte swizzle (layout type 4), 8-row groups of 512 bytes
+constexpr uint32_t kSdescHi64 = (512u >> 4) | (1u << (46 - 32)) | (4u << (61 - 32));
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
 
 // S = Q K^T: one MMA per 32 bytes of the head dimension; the operands' low
 // descriptor words advance by the same offset in Q and K (16-byte units)
-// (ACC0: the first MMA accumulates too; used for O += P V with P in shared memory)
-template <int DT, int CHUNK_BYTES, bool ACC0 = false, size_t... KK>
+// (ACC0: the first MMA accumulates too; used for O += P V with P in shared
+// memory; KPC: MMAs per swizzle chunk of a row; HI: descriptor high word)
+template <int DT, int CHUNK_BYTES, bool ACC0 = false, int KPC = 4, uint32_t HI = kSdescHi,
+          size_t... KK>
 __device__ __forceinline__ void issue_s_mmas(uint32_t tS, uint32_t qlo, uint32_t klo, uint32_t idS,
                                              std::index_sequence<KK...>) {
   (ptx::mma_ss_lo<DT == DT_E4M3, ((KK > 0 || ACC0) ? 1 : 0),
-                  (uint32_t)((((int)KK >> 2) * CHUNK_BYTES + ((int)KK & 3) * 32) >> 4), kSdescHi>(
+                  (uint32_t)((((int)KK / KPC) * CHUNK_BYTES + ((int)KK % KPC) * 32) >> 4), HI>(
        tS, qlo, klo, idS),
    ...);
 }
@@ -487,8 +494,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       // S = Q K^T into tS and O += P V with P read from tS (accumulating),
       // from the low descriptor words of the operands' shared-memory tiles
       auto issue_s = [&](uint32_t tS, uint32_t qlo, uint32_t klo) {
-        issue_s_mmas<DT, C::CHUNK_BYTES>(tS, qlo, klo, idS,
-                                         std::make_index_sequence<C::ROWB / 32>{});
+        issue_s_mmas<DT, C::CHUNK_BYTES, false, C::SWZ / 32, C::SWZ == 128 ? kSdescHi : kSdescHi64>(
+            tS, qlo, klo, idS, std::make_index_sequence<C::ROWB / 32>{});
       };
       // FP8: 32 keys per MMA (V^T tile, K-major); 16-bit: 16 keys per MMA
       constexpr int PV_MMAS = DT == DT_E4M3 ? 4 : 8;
@@ -1054,9 +1061,21 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
             ok = warp_wait_bar(bar(B_PFREEB + 2 * s + (n & 1)), (n >> 1) & 1, ctl);
             if (!ok) break;
             ptx::tc_fence_after();
-            static_assert(D % 128 == 0, "O rescale in pairs of 64-column loads");
+            if constexpr (D == 64) {
+              uint32_t oa[64];
+              ptx::tmem_ld_x64(tO, oa);
+#pragma unroll
+              for (int c = 0; c < 64; c += 2) {
+                float a0, a1;
+                ptx::fma2(a0, a1, __uint_as_float(oa[c]), __uint_as_float(oa[c + 1]), alpha, alpha,
+                          0.f, 0.f);
+                oa[c] = __float_as_uint(a0);
+                oa[c + 1] = __float_as_uint(a1);
+              }
+              ptx::tmem_st_x64(tO, oa);
+            }
 #pragma unroll 1
-            for (int cb = 0; cb < D; cb += 128) {
+            for (int cb = 0; cb + 128 <= D; cb += 128) {
               uint32_t oa[64], ob[64];
               ptx::tmem_ld_x64_nowait(tO + cb, oa);
               ptx::tmem_ld_x64_nowait(tO + cb + 64, ob);

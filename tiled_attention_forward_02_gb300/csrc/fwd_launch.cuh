@@ -45,9 +45,7 @@ template <int DT>
 int launch_fwd_dt(int d, int causal, const CUtensorMap& q, const CUtensorMap& k,
                   const CUtensorMap& v, const FwdParams& p, int grid, cudaStream_t stream) {
   switch (d) {
-    case 64:
-      if constexpr (DT == DT_E4M3) return ATTN_ERR_UNSUPPORTED;
-      else return launch_fwd_d<DT, 64>(causal, q, k, v, p, grid, stream);
+    case 64: return launch_fwd_d<DT, 64>(causal, q, k, v, p, grid, stream);
     case 128: return launch_fwd_d<DT, 128>(causal, q, k, v, p, grid, stream);
     case 256: return launch_fwd_d<DT, 256>(causal, q, k, v, p, grid, stream);
     default: return ATTN_ERR_UNSUPPORTED;

@@ -44,6 +44,7 @@ int device_attrs(int dev, int* sm_count, int* cc_major, int* cc_minor);
 int check_common(int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int causal, float scale);
 // BSHD tensor [B, N, H, d] as a 4-D tensor map (d, H, N, B) with a box of
 // `heads` heads x 128 / heads rows x `inner` elements, 128-byte swizzle
+// (64-byte swizzle for 64-byte rows: inner x element size = 64)
 int map_bshd(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* base, int B, int64_t N,
              int H, int d, int inner, int heads);
 // forward parameters and persistent grid size for a problem
