@@ -359,15 +359,13 @@ extern "C" int attn_prep_fp8_qkv(const void* q, const void* k, const void* v, vo
   // optional rotation and transform; V: transposed codes)
   PrepJobs J{};
   int n = 0;
-  long long tiles = 0;
   auto add = [&](const void* x, void* x8, float* ds, int H, int64_t N, const int8_t* sg,
                  int group, int tr, bool rot) -> int {
     if (N == 0) return ATTN_OK;
     const int r = map_prep(&J.map[n], x, B, N, H, d);
     if (r != ATTN_OK) return r;
     J.job[n] = prep_job(x8, ds, B, H, (int)N, sg, group, tr, rot ? rope_cos : nullptr,
-                        rot ? rope_sin : nullptr, tiles);
-    tiles += (long long)B * J.job[n].nb * H;
+                        rot ? rope_sin : nullptr);
     ++n;
     return ATTN_OK;
   };
@@ -377,7 +375,7 @@ extern "C" int attn_prep_fp8_qkv(const void* q, const void* k, const void* v, vo
     return rc;
   J.n_jobs = n;
   J.any_transpose = Nk > 0 ? 1 : 0;
-  J.n_tiles = tiles;
+  prep_order(J);
   J.sched = prep_slot(st);
   return launch_prep_jobs(J, d, st->sm_count, st->status, static_cast<cudaStream_t>(stream));
 }

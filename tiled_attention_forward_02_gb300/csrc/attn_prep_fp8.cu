@@ -103,7 +103,7 @@ __device__ __forceinline__ int tr_word(int e, int kw) {
 
 // A launch walks the tiles of up to three tensors (Q, K, V of one attention
 // call) one tensor after the other, so that the ramp-up and the tail of a
-// persistent launch (about 7 us) are paid once per step instead of per tensor.
+// persistent launch are paid once per step instead of per tensor.
 // Each CTA's first NS tiles are fixed (tile blockIdx + s * grid); every later
 // tile is claimed from a counter (J.sched[0]), so that CTAs on faster SMs take
 // more tiles and all of them end within about one tile of each other. The
@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   static_assert(NS <= 4, "tail layout");
   uint64_t* bars = reinterpret_cast<uint64_t*>(tail);          // [NS] tile landed
   float* s_amax = reinterpret_cast<float*>(tail + 32);         // [2][8], 16-byte aligned
-  long long* s_tile = reinterpret_cast<long long*>(tail + 96); // [NS] tile of a stage
+  // [NS] tile of a stage as (tensor, head, block, batch), decoded once by the
+  // thread that issues its copy; tensor -1 is the end mark
+  int4* s_info = reinterpret_cast<int4*>(tail + 96);
   auto bar = [&](int i) { return ptx::smem_addr(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -142,9 +144,9 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   const long long G = gridDim.x;
   // tensor of tile t, its parameters and its tensor map (constant indices
   // into the kernel parameter)
-  auto job_of = [&](long long t) {
-    return (J.n_jobs > 1 && t >= J.job[1].tile0 ? 1 : 0) +
-           (J.n_jobs > 2 && t >= J.job[2].tile0 ? 1 : 0);
+  auto locate = [&](long long t, int& jj, long long& tl) {
+    jj = (J.n_jobs > 1 && t >= J.tile0[1] ? 1 : 0) + (J.n_jobs > 2 && t >= J.tile0[2] ? 1 : 0);
+    tl = t - J.tile0[jj];
   };
   auto job = [&](int jj) { return jj == 0 ? J.job[0] : jj == 1 ? J.job[1] : J.job[2]; };
   auto map_of = [&](int jj) { return jj == 0 ? &J.map[0] : jj == 1 ? &J.map[1] : &J.map[2]; };
@@ -160,17 +162,18 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   // the stage's phase, so a thread that saw the phase complete reads it
   auto issue = [&](int st, long long t) {
     if (t >= n_tiles) {
-      s_tile[st] = -1;
+      s_info[st] = make_int4(-1, 0, 0, 0);
       ptx::mbar_arrive(bar(st));
       return;
     }
-    s_tile[st] = t;
-    const int jj = job_of(t);
+    int jj;
+    long long tl;
+    locate(t, jj, tl);
     const PrepJob jb = job(jj);
-    const long long tl = t - jb.tile0;
     const int th = (int)(tl % jb.H);
     const long long r = tl / jb.H;
     const int tblk = (int)(r % jb.nb), tb = (int)(r / jb.nb);
+    s_info[st] = make_int4(jj, th, tblk, tb);
     ptx::mbar_arrive_expect_tx(bar(st), PC::TILE_BYTES);
     ptx::tma_load_4d(sbase + st * PC::TILE_BYTES, map_of(jj), bar(st), 0, th, tblk * 128, tb);
   };
@@ -204,9 +207,9 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
       while (!(ok = ptx::mbar_try_wait_sleep(bar(st), (uint32_t)((k / NS) & 1), 100000)))
         if (clock64() - t0 > kPrepWaitCycles) break;
     }
-    const long long t = ok ? s_tile[st] : 0;
-    if (t < 0) break;
-    const PrepJob jb = job(job_of(t));
+    const int4 info = ok ? s_info[st] : make_int4(0, 0, 0, 0);
+    if (info.x < 0) break;
+    const PrepJob jb = job(info.x);
     const int H = jb.H, N = jb.N, nb = jb.nb, Npad = jb.Npad;
     const int transpose_out = jb.transpose_out, sign_group = jb.sign_group;
     uint8_t* __restrict__ x8 = jb.x8;
@@ -214,10 +217,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     const int8_t* __restrict__ signs = jb.signs;
     const float* __restrict__ rope_cos = jb.rope_cos;
     const float* __restrict__ rope_sin = jb.rope_sin;
-    const long long tl = t - jb.tile0;
-    const int h = (int)(tl % H);
-    const long long rr = tl / H;
-    const int blk = (int)(rr % nb), b = (int)(rr / nb);
+    const int h = info.y, blk = info.z, b = info.w;
     // (a thread whose wait gave up reads stale data; the block leaves at the
     // amax barrier below, before anything is stored)
     const int n0 = blk * 128 + r0;   // token of iteration 0
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
         // wait (bounded) for the copies this CTA still has in flight
         for (long long kk = k; kk < k + NS; ++kk) {
           const int sk = (int)(kk % NS);
-          if (s_tile[sk] < 0) break;
+          if (s_info[sk].x < 0) break;
           const long long t0 = clock64();
           while (!ptx::mbar_try_wait(bar(sk), (uint32_t)((kk / NS) & 1)))
             if (clock64() - t0 > kPrepWaitCycles) break;
@@ -543,8 +543,8 @@ int launch_prep_d(int d, const PrepJobs& J, int sm_count, float* tensor_amax, un
 }
 
 PrepJob prep_job(void* x8, float* descale, int B, int H, int N, const int8_t* signs,
-                 int sign_group, int transpose_out, const float* rope_cos, const float* rope_sin,
-                 long long tile0) {
+                 int sign_group, int transpose_out, const float* rope_cos,
+                 const float* rope_sin) {
   PrepJob jb{};
   jb.x8 = static_cast<uint8_t*>(x8);
   jb.descale = descale;
@@ -557,9 +557,16 @@ PrepJob prep_job(void* x8, float* descale, int B, int H, int N, const int8_t* si
   jb.nb = (N + 127) / 128;
   jb.Npad = (N + 15) / 16 * 16;
   jb.transpose_out = transpose_out;
-  jb.tile0 = tile0;
-  (void)B;
+  jb.n_tiles = (long long)B * jb.nb * H;
   return jb;
+}
+
+void prep_order(PrepJobs& J) {
+  J.n_tiles = 0;
+  for (int i = 0; i < 3; ++i) {
+    J.tile0[i] = J.n_tiles;
+    if (i < J.n_jobs) J.n_tiles += J.job[i].n_tiles;
+  }
 }
 
 int launch_prep_jobs(const PrepJobs& J, int d, int sm_count, unsigned int* status,
@@ -577,10 +584,10 @@ int launch_prep_fp8(const CUtensorMap& map_x, void* x8, float* descale, int B, i
   PrepJobs J{};
   J.sched = sched;
   J.map[0] = map_x;
-  J.job[0] = prep_job(x8, descale, B, H, N, signs, sign_group, transpose_out, rope_cos, rope_sin, 0);
+  J.job[0] = prep_job(x8, descale, B, H, N, signs, sign_group, transpose_out, rope_cos, rope_sin);
   J.n_jobs = 1;
   J.any_transpose = transpose_out;
-  J.n_tiles = (long long)B * J.job[0].nb * H;
+  prep_order(J);
   if (!per_tensor) return launch_prep_jobs(J, d, sm_count, status, stream);
   if (rope_cos) return ATTN_ERR_UNSUPPORTED;
   // the tensor amax is accumulated in descale[0] and read from there

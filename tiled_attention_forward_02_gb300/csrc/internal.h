@@ -71,33 +71,36 @@ int launch_splitkv_merge(const float* o_part, const float* lse_part, void* o, fl
 
 // One tensor of an FP8 prep launch (per-block mode): codes x8 (BSHD, or
 // [B, H, d, Npad] when transpose_out), descales [B, H, nb], optional signs
-// [H / sign_group, d] and rotary tables [N, d/2]; tile0 is its first tile in
-// the launch (tiles of a tensor: heads fastest, then 128-token blocks, then
-// batch).
+// [H / sign_group, d] and rotary tables [N, d/2]; n_tiles = B x nb x H tiles
+// (heads fastest, then 128-token blocks, then batch).
 struct PrepJob {
   uint8_t* x8;
   float* descale;
   const int8_t* signs;
   const float* rope_cos;
   const float* rope_sin;
-  long long tile0;
+  long long n_tiles;
   int sign_group, H, N, nb, Npad, transpose_out;
 };
 // up to three tensors in one launch; map[i]: tensor i's bf16 input as
 // (d, H, N, B), box d x 1 x 128 x 1, no swizzle; sched: the launch's tile
 // counter and finished-CTA count, both zero before the launch (the kernel
 // leaves them zero)
+// Launch tile t is tile t - tile0[j] of tensor j, tile0[j] <= t < tile0[j + 1]
+// (the tensors one after the other).
 struct PrepJobs {
   CUtensorMap map[3];
   PrepJob job[3];
   int n_jobs;
   int any_transpose;
   long long n_tiles;
+  long long tile0[3];
   unsigned long long* sched;
 };
 PrepJob prep_job(void* x8, float* descale, int B, int H, int N, const int8_t* signs,
-                 int sign_group, int transpose_out, const float* rope_cos, const float* rope_sin,
-                 long long tile0);
+                 int sign_group, int transpose_out, const float* rope_cos, const float* rope_sin);
+// n_tiles and tile0 of J from its jobs
+void prep_order(PrepJobs& J);
 int launch_prep_jobs(const PrepJobs& J, int d, int sm_count, unsigned int* status,
                      cudaStream_t stream);
 
