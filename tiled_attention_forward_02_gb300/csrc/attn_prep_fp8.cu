@@ -170,9 +170,12 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     long long tl;
     locate(t, jj, tl);
     const PrepJob jb = job(jj);
-    const int th = (int)(tl % jb.H);
-    const long long r = tl / jb.H;
-    const int tblk = (int)(r % jb.nb), tb = (int)(r / jb.nb);
+    // (a launch holds fewer than 2^31 tiles: 32-bit division)
+    const unsigned ut = (unsigned)tl, uh = (unsigned)jb.H, unb = (unsigned)jb.nb;
+    const unsigned r = ut / uh;
+    const int th = (int)(ut - r * uh);
+    const int tb = (int)(r / unb);
+    const int tblk = (int)(r - (unsigned)tb * unb);
     s_info[st] = make_int4(jj, th, tblk, tb);
     ptx::mbar_arrive_expect_tx(bar(st), PC::TILE_BYTES);
     ptx::tma_load_4d(sbase + st * PC::TILE_BYTES, map_of(jj), bar(st), 0, th, tblk * 128, tb);
@@ -521,6 +524,8 @@ template <int D, int MODE, bool ROPE>
 int launch_prep_instance(const PrepJobs& J, int sm_count, float* tensor_amax,
                          unsigned int* status, cudaStream_t stream) {
   auto kern = prep_fp8_kernel<D, MODE, ROPE>;
+  // the kernel decodes tile indices in 32-bit arithmetic
+  if (J.n_tiles >= ((long long)1 << 31)) return ATTN_ERR_UNSUPPORTED;
   const int smem = PrepCfg<D>::smem_bytes(J.any_transpose);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prep)");
