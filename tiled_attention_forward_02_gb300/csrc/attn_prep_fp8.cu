@@ -142,14 +142,13 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
   const int r0 = warp * 16 + ITERS * rsub;
   const long long n_tiles = J.n_tiles;
   const long long G = gridDim.x;
-  // tensor of tile t, its parameters and its tensor map (constant indices
-  // into the kernel parameter)
+  // tensor of tile t; its parameters and tensor map are read in place from
+  // the kernel parameter
   auto locate = [&](long long t, int& jj, long long& tl) {
     jj = (J.n_jobs > 1 && t >= J.tile0[1] ? 1 : 0) + (J.n_jobs > 2 && t >= J.tile0[2] ? 1 : 0);
     tl = t - J.tile0[jj];
   };
-  auto job = [&](int jj) { return jj == 0 ? J.job[0] : jj == 1 ? J.job[1] : J.job[2]; };
-  auto map_of = [&](int jj) { return jj == 0 ? &J.map[0] : jj == 1 ? &J.map[1] : &J.map[2]; };
+  auto map_of = [&](int jj) { return &J.map[jj]; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) ptx::mbar_init(bar(i), 1);
@@ -169,7 +168,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     int jj;
     long long tl;
     locate(t, jj, tl);
-    const PrepJob jb = job(jj);
+    const PrepJob& jb = J.job[jj];
     // (a launch holds fewer than 2^31 tiles: 32-bit division)
     const unsigned ut = (unsigned)tl, uh = (unsigned)jb.H, unb = (unsigned)jb.nb;
     const unsigned r = ut / uh;
@@ -212,7 +211,7 @@ __global__ void __launch_bounds__(256, PrepCfg<D>::CTAS_PER_SM)
     }
     const int4 info = ok ? s_info[st] : make_int4(0, 0, 0, 0);
     if (info.x < 0) break;
-    const PrepJob jb = job(info.x);
+    const PrepJob& jb = J.job[info.x];   // (read in place from the kernel parameter)
     const int H = jb.H, N = jb.N, nb = jb.nb, Npad = jb.Npad;
     const int transpose_out = jb.transpose_out, sign_group = jb.sign_group;
     uint8_t* __restrict__ x8 = jb.x8;
