@@ -875,7 +875,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::NTHREADS, 1)
       const int m_s = U.m0 + s * (128 / G);   // first query position of this tile
       const int row = m_s + r / G;            // query position of this thread's row
       const int hrow = U.hq + r % G;          // query head of this thread's row
-      const int ns = U.n_s[s];
+      const int ns = s == 0 ? U.n_s[0] : U.n_s[1];   // (no dynamic index: U stays in registers)
 
       float qd = 1.f, vref = 1.f;
       const float* kd_row = nullptr;
