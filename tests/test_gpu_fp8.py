@@ -269,9 +269,12 @@ def test_fp8_full_workload_every_row_vs_dequantised_oracle(gpu_lib):
 
 # --- per-tensor baseline ------------------------------------------------------
 
-@pytest.mark.parametrize("d", [64, 128, 256])
-def test_prep_per_tensor_bit_exact_without_transform(gpu_lib, d):
-    B, N, H = 2, 1000, 3
+@pytest.mark.parametrize("d,N,H", [(64, 1000, 3), (128, 1000, 3), (256, 1000, 3),
+                                   (128, 4000, 16)])
+def test_prep_per_tensor_bit_exact_without_transform(gpu_lib, d, N, H):
+    """Small cases, and one with several times more tiles than CTAs (most
+    tiles of both passes claimed from the launch's counter)."""
+    B = 2
     x, _, _ = synth.attn_inputs(B, N, N, H, H, d, dtype=torch.bfloat16, seed=21,
                                 outlier_frac=1e-3)
     codes, ds = gpu_lib.attn_prep_fp8_per_tensor(x.cuda())
