@@ -27,8 +27,9 @@
 // every rounding midpoint, see the quantisation step), else of y * (448 /
 // amax) with the reciprocal rounded once per block.  It
 // reads each bf16 element once and writes one byte per element, an HBM-bound
-// amount of work; at two CTAs of 8 warps per SM (register and shared-memory
-// limits) the kernel itself is bound by instruction latency, not bandwidth.
+// amount of work (two CTAs of 8 warps per SM, register and shared-memory
+// limits); per-tile scalar work on the thread that issues the copies delays
+// its warp at every tile barrier, so it is kept to a minimum.
 //
 // Two variants share the kernel:
 // * rotary embedding before the transform (the summary card notes that the
