@@ -123,6 +123,13 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *            Apply it to Q and K with the same signs per key/value head
  *            (Q's sign_heads = Hkv); never to V.
  *   d        64, 128 or 256
+ * Every prep entry point (this one, attn_prep_fp8_per_tensor,
+ * attn_prep_fp8_rope, attn_prep_fp8_qkv) hands its launch's tiles out
+ * through one of 64 device counters that the library takes in turn and each
+ * launch leaves at zero: at most 64 prep launches may run at the same time
+ * (on different streams). A launch holds fewer than 2^31 tiles of 128 tokens
+ * (B x ceil(N/128) x H summed over its tensors); larger ones return
+ * ATTN_ERR_UNSUPPORTED.
  */
 int attn_prep_fp8(const void* x, void* x8, float* descale, int B, int H, int64_t N, int d,
                   const int8_t* signs, int sign_heads, int transpose_out, void* stream);
